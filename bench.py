@@ -1,0 +1,314 @@
+"""Benchmark of one DSpark round (draft -> schedule -> verify) on GB300.
+
+Default workload: the DeepSeek-scale configuration (R = 128 requests,
+gamma = 16, V = 129280, Markov rank 256, bf16, temperature 1, causal
+scheduler), synthetic inputs from the seeded generators, built on the device.
+
+One "step" is one whole round through the library's public C ABI
+(dspark_round). `value` is drafted positions per second (R * gamma / round
+latency) from CUDA events on the launching stream, inputs resident in HBM,
+L2 flushed (256 MiB write) between steps outside the timed events. `e2e`
+is the same metric through the same C ABI with the step's inputs copied from
+pinned host memory and the results copied back inside the timed region.
+
+--impl reference times the oracle (the plain CPU implementation) on a bounded
+sample of the same workload on the host cores.
+
+Multi-GPU: the path shards by request with no exchange on the data path
+(replicas only): under torchrun every rank runs its own round on its own GPU,
+timing is the max over ranks and `value` sums all ranks' positions.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify round latency (µs) & positions/s at R=128,γ=16,V=129280; %HBM roof"
+FALLBACK_HBM = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM, "fallback"
+
+
+def algorithmic_bytes(cfg, L):
+    """Bytes each pass must touch once (re-reads excluded)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    draft = cfg.R * cfg.gamma * cfg.V * e + cfg.rank * cfg.V * e + cfg.R * cfg.gamma * cfg.rank * e
+    verify = int((L + 1).sum()) * cfg.V * e
+    return draft, verify
+
+
+def cpu_baseline(cfg, n_req, timeout=600):
+    """Times the oracle on `n_req` requests in a single-threaded child process."""
+    code = (
+        "import time, json, sys; sys.path.insert(0, %r)\n"
+        "import workloads as W\n"
+        "from oracle.round import run_round\n"
+        "cfg = W.CONFIGS[%r]\n"
+        "req = list(range(%d))\n"
+        "inp = W.oracle_inputs(cfg, req)\n"
+        "t = time.perf_counter(); run_round(inp, requests=req); dt = time.perf_counter() - t\n"
+        "print(json.dumps({'seconds': dt}))\n" % (ROOT, cfg.name, n_req))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=timeout)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    dt = json.loads(out.stdout.strip().splitlines()[-1])["seconds"]
+    pos = n_req * cfg.gamma
+    return {"value": pos / dt, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_req} of {cfg.R} requests x gamma={cfg.gamma} (full round: schedule over all "
+                      f"requests, draft + verify of the sampled ones), single thread, {dt:.1f} s"}
+
+
+class ClockSampler:
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self, rank):
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0] or "0"
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(rank if not dev.isdigit() else dev),
+                                          f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="ds")
+    ap.add_argument("--temperature", type=float, default=None)
+    ap.add_argument("--cpu-requests", type=int, default=12)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import workloads as W
+    cfg = W.CONFIGS[args.config]
+    if args.temperature is not None:
+        cfg = W.with_(cfg, T=args.temperature)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    workload = (f"{cfg.name}: R={cfg.R} gamma={cfg.gamma} V={cfg.V} rank={cfg.rank} {cfg.dtype} "
+                f"T={cfg.T} scheduler={['causal', 'lagged', 'all'][cfg.mode]}")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ref_steps = []
+        for _ in range(max(1, args.steps)):
+            b = cpu_baseline(cfg, max(1, args.cpu_requests // 4))
+            ref_steps.append(b)
+        v = sum(x["value"] for x in ref_steps) / len(ref_steps)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "positions/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * cfg.R * cfg.gamma / v, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": workload},
+                "cpu_baseline": {"value": v, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                                 "sample": ref_steps[0]["sample"]},
+                "e2e": {"value": v, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import numpy as np
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_draft_seq_gb300 import dspark
+
+    tests_dir = os.path.join(ROOT, "tests")
+    sys.path.insert(0, tests_dir)
+    from gpu_harness import device_inputs
+    inp = device_inputs(cfg, dev)
+    R, gamma, V = cfg.R, cfg.gamma, cfg.V
+    dt_code = dspark.BF16 if cfg.dtype == "bf16" else dspark.FP32
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dt_code, cfg.n_table, dev)
+    out = dspark.RoundOutputs(R, gamma, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def one_round():
+        dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                      inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+
+    for _ in range(max(3, args.warmup)):
+        one_round()
+    torch.cuda.synchronize()
+    st = dspark.device_status(ws)
+    if st != dspark.OK:
+        raise RuntimeError(f"device status {dspark.status_string(st)}")
+    launches_per_round = dspark.last_launch_count()
+
+    # stage timing (draft / schedule / verify separately, same stream)
+    def time_stage(fn, n):
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    t_draft = time_stage(lambda: dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"],
+                                                         inp["T"], inp["seed"], out.tokens, out.q_tok,
+                                                         out.q_stats, ws), max(3, args.steps // 4))
+    t_sched = time_stage(lambda: dspark.schedule(inp["conf"], inp["conf_lag"], inp["sps"], inp["mode"],
+                                                 out.sched_len, out.K, out.tau_theta, ws),
+                         max(3, args.steps // 4))
+    t_verify = time_stage(lambda: dspark.verify(inp["target"], inp["base"], inp["anchor"], inp["W1"],
+                                                inp["W2"], out.tokens, out.q_tok, out.q_stats, out.sched_len,
+                                                inp["T"], inp["seed"], out.out_tokens, out.accepted_len,
+                                                out.p_tok, ws), max(3, args.steps // 4))
+
+    clocks = ClockSampler()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start(rank)
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one_round()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = float(np.sum(times)) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * R * gamma / (ms * 1e-3)
+
+    # end to end through the same C ABI from pinned host buffers
+    host = {k: inp[k].cpu().pin_memory() for k in ("base", "target", "anchor", "conf") }
+    if inp["conf_lag"] is not None:
+        host["conf_lag"] = inp["conf_lag"].cpu().pin_memory()
+    res_host = {k: torch.empty_like(getattr(out, k), device="cpu").pin_memory()
+                for k in ("out_tokens", "accepted_len", "sched_len")}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        dspark.round_(dev_in["base"], dev_in["target"], dev_in["anchor"], inp["W1"], inp["W2"],
+                      dev_in["conf"], dev_in.get("conf_lag"), inp["sps"], inp["mode"], inp["T"],
+                      inp["seed"], out, ws)
+        for k, v in res_host.items():
+            v.copy_(getattr(out, k), non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_t = []
+    for _ in range(max(3, args.steps // 2)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_t.append(a.elapsed_time(b))
+    e2e_ms = float(np.mean(e2e_t))
+
+    L = out.sched_len.cpu().numpy()
+    A = out.accepted_len.cpu().numpy()
+    peak, peak_kind = peaks()
+    bd, bv = algorithmic_bytes(cfg, L)
+    draft_gbs = bd / (t_draft * 1e-3) / 1e9
+    verify_gbs = bv / (t_verify * 1e-3) / 1e9
+    dominant = "draft" if t_draft >= t_verify else "verify"
+    ach = draft_gbs if dominant == "draft" else verify_gbs
+    traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": ach / peak,
+                     "traffic": traffic,
+                     "algorithmic_bytes": bd if dominant == "draft" else bv,
+                     "draft_frac": draft_gbs / peak, "verify_frac": verify_gbs / peak},
+        "round_stats": {"scheduled_positions": int(L.sum()), "accepted": int(A.sum()),
+                        "emitted": int((A + 1).sum()),
+                        "scheduled_positions_per_s": world * int(L.sum()) / (ms * 1e-3),
+                        "emitted_tokens_per_s": world * int((A + 1).sum()) / (ms * 1e-3)},
+        "e2e": {"value": world * R * gamma / (e2e_ms * 1e-3), "unit": "positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": launches_per_round * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_requests)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * dspark.h -- C ABI of the DSpark per-round hot path on one GB300 (sm_103a).
+ *
+ * One decoding round of DSpark speculative decoding, as the pages describe it
+ * ("DSpark: Aceleração da inferência de LLM com speculative decoding [pdf]",
+ * GeekNews, section "Arquitetura - dois componentes complementares"):
+ *   1. draft   -- sequential Markov-head stage over the parallel backbone's
+ *                 base logits: for k = 1..gamma, bias = W1[prev] . W2 is added
+ *                 to base logits of position k, a tempered softmax over the
+ *                 whole vocabulary is formed and token k is sampled;
+ *   2. schedule-- confidence-scheduled verification lengths: prefix-survival
+ *                 products, a global descending merge of all R x gamma
+ *                 candidates, greedy admission against a throughput table
+ *                 with early stop ("Verificação com agendamento por
+ *                 confiança", "Hardware-Aware Prefix Scheduler"), or the
+ *                 production lagged variant ("Aplicação prática do scheduler");
+ *   3. verify  -- lossless speculative sampling: accept x_k with probability
+ *                 min(1, p/q), resample the first rejection from
+ *                 normalize(max(0, p - q)), or draw a bonus token when every
+ *                 scheduled token is accepted ("Definição do problema").
+ * The parallel backbone, confidence head and target forward pass are outside
+ * this library: their outputs (base logits, confidences, target logits) are
+ * inputs.
+ *
+ * Conventions (all entry points):
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, row-major,
+ *     densely packed, at least 16-byte aligned. The library allocates no
+ *     memory and keeps no pointer after a call returns.
+ *   - `dtype` selects the element type of base logits, target logits, W1 and
+ *     W2: DSPARK_BF16 (bf16 bit patterns) or DSPARK_FP32. Everything else is
+ *     int32 / float32 / float64 as declared.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). Only host-checkable argument errors are returned
+ *     synchronously; nothing is launched in that case.
+ *   - Errors found on the device (non-finite inputs, a token id out of range,
+ *     a bounded wait that ran out) set a sticky status word inside the
+ *     workspace; read it with dspark_device_status(). Nothing aborts, traps
+ *     or prints.
+ *   - Randomness: one uniform per decision, U(seed, r, k, purpose), from
+ *     Philox4x64-10 (Salmon et al., SC'11) with key (seed, 0x44535041524B0000)
+ *     and counter (r, k, purpose, 0), u = (2*(w0 >> 12) + 1) * 2^-53;
+ *     purposes DRAFT=0 (r, k), ACCEPT=1 (r, k), RESID=2 (r, j), BONUS=3
+ *     (r, L_r + 1). Same inputs and seed give bit-identical outputs.
+ *   - Sampling is inverse-CDF in vocabulary order: the smallest v with
+ *     u * Z < sum_{i<=v} w_i. Temperature 0 is greedy (argmax, lowest index on
+ *     ties) for both the draft and the target.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* dspark_stream_t;
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1, /* bad shape, null pointer, unsupported combination */
+  DSPARK_ERR_NONFINITE = 2,   /* NaN/Inf confidence or cost-table entry (device) */
+  DSPARK_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+  DSPARK_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  DSPARK_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (device) */
+  DSPARK_ERR_RANGE = 6        /* a token id outside [0, V) was read (device) */
+} dspark_status;
+
+typedef enum { DSPARK_FP32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum {
+  DSPARK_SCHED_CAUSAL = 0, /* greedy admission with early stop */
+  DSPARK_SCHED_LAGGED = 1, /* K from lagged confidences (argmax, no early stop), top K of current */
+  DSPARK_SCHED_ALL = 2     /* verify every drafted position (scheduler off) */
+} dspark_sched_mode;
+
+/* Bytes of device workspace every entry point below needs for these sizes.
+ * One workspace may be reused by consecutive calls on one stream; calls that
+ * may overlap on the GPU need separate workspaces. Alignment: 256 bytes. */
+size_t dspark_workspace_bytes(int32_t R, int32_t gamma, int32_t V, int32_t rank,
+                              int32_t dtype, int32_t n_table);
+
+/* Clears the workspace's status word (async on `stream`). Call once after
+ * allocating a workspace; every entry point below leaves earlier errors in
+ * place (sticky) until this is called again. */
+dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes,
+                                    dspark_stream_t stream);
+
+/*
+ * Sequential drafting stage with the low-rank Markov head (GeekNews page,
+ * "Geração semiautorregressiva": "Etapa sequencial" and "Head de Markov";
+ * the anchor is the first prediction position, "Etapa paralela").
+ *
+ *   base_logits  [R, gamma, V] dtype   row k-1 = base logits of block position k
+ *   anchor       [R] int32             the target's last sampled token
+ *   W1           [V, rank] dtype       Markov factor: bias(prev) = W1[prev, :] . W2
+ *   W2           [rank, V] dtype
+ *   temperature  >= 0; softmax((base + bias) / T); 0 = greedy
+ *   draft_tokens [R, gamma] int32 out  x_{r,k}; prev of position k>1 is x_{r,k-1}
+ *   q_tok        [R, gamma] float out  Q_k(x_k), the draft probability of x_k
+ *   q_stats      [R, gamma, 2] float out  (M, Z): Q_k(v) = 2^((l_v - M) log2(e)/T) / Z
+ *                                         (greedy: (max l, 1))
+ * Requirements: R >= 1, gamma >= 1, V >= 1, rank >= 1. The bf16 tensor-core
+ * path is used when dtype = BF16, rank % 16 == 0, rank <= 256, V % 8 == 0;
+ * other shapes run on CUDA cores with the same results up to rounding.
+ */
+dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32_t rank,
+                                      int32_t dtype, const void* base_logits,
+                                      const int32_t* anchor, const void* W1, const void* W2,
+                                      float temperature, uint64_t seed,
+                                      int32_t* draft_tokens, float* q_tok, float* q_stats,
+                                      void* workspace, size_t workspace_bytes,
+                                      dspark_stream_t stream);
+
+/*
+ * Hardware-aware prefix scheduler (GeekNews page, "Verificação com
+ * agendamento por confiança": "Hardware-Aware Prefix Scheduler" and
+ * "Calibração posterior"; production variant in "Aplicação prática do
+ * scheduler").
+ *
+ *   conf        [R, gamma] float   c_{r,k}, clamped to [0, 1]; non-finite -> DSPARK_ERR_NONFINITE
+ *   conf_lagged [R, gamma] float   confidences of two rounds earlier (LAGGED only, else NULL)
+ *   sps_table   [n_table] float    SPS(B) at B = i + 1 batch tokens (finite)
+ *   mode        dspark_sched_mode
+ *   sched_len   [R] int32 out      L_r, the verified prefix length of request r
+ *   K           [1] int32 out      admitted candidates (sum of L_r)
+ *   tau_theta   [2] double out     expected tokens tau and Theta = tau * SPS(R + K)
+ * Arithmetic (fixed so every implementation agrees bit for bit):
+ *   a_{r,j} = fl32(a_{r,j-1} * c_{r,j}), a_{r,0} = 1; candidates ordered by a
+ *   descending, ties by flat index r*gamma + j - 1; after i admissions
+ *   tau_i = R + S_i * 2^-40 with S_i the sum of floor(a * 2^40 + 1/2),
+ *   Theta_i = tau_i * SPS[R + i - 1] (float64). CAUSAL admits candidate i+1
+ *   while R + i + 1 <= n_table and Theta_{i+1} >= Theta_i. LAGGED takes K as
+ *   the smallest argmax of Theta_i (lagged confidences), i <= min(R gamma,
+ *   n_table - R), then admits the top K current candidates. R > n_table admits
+ *   nothing (K = 0, Theta reported 0). ALL sets L_r = gamma.
+ * Requirements: R * gamma <= 65536.
+ */
+dspark_status dspark_schedule(int32_t R, int32_t gamma, const float* conf,
+                              const float* conf_lagged, const float* sps_table,
+                              int32_t n_table, int32_t mode, int32_t* sched_len,
+                              int32_t* K, double* tau_theta, void* workspace,
+                              size_t workspace_bytes, dspark_stream_t stream);
+
+/*
+ * Lossless speculative-sampling verification (GeekNews page, "Definição do
+ * problema" and the decoding-cycle paragraph: E, F accepted, G rejected and
+ * replaced by a corrected G*).
+ *
+ *   target_logits [R, gamma+1, V] dtype  row k = target logits after the anchor and k draft tokens
+ *   base_logits, anchor, W1, W2           as for drafting (the draft distribution Q_j of the first
+ *                                          rejected position is recomputed for the residual)
+ *   draft_tokens, q_tok, q_stats          outputs of dspark_draft_sequential
+ *   sched_len     [R] int32               L_r from dspark_schedule (0..gamma)
+ *   out_tokens    [R, gamma+1] int32 out  x_1..x_{A_r} then the corrected/bonus token; -1 after
+ *   accepted_len  [R] int32 out           A_r in [0, L_r]
+ *   p_tok         [R, gamma] float out    P_{k-1}(x_k) for k <= L_r, 0 beyond
+ * Rule: accept x_k iff u_ACCEPT < p/q (strict); at the first rejection j draw
+ * from normalize(max(0, P_{j-1} - Q_j)) (from P_{j-1} if that has no mass);
+ * if all L_r are accepted draw the bonus from P_{L_r}.
+ */
+dspark_status dspark_verify(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                            const void* target_logits, const void* base_logits,
+                            const int32_t* anchor, const void* W1, const void* W2,
+                            const int32_t* draft_tokens, const float* q_tok,
+                            const float* q_stats, const int32_t* sched_len,
+                            float temperature, uint64_t seed, int32_t* out_tokens,
+                            int32_t* accepted_len, float* p_tok, void* workspace,
+                            size_t workspace_bytes, dspark_stream_t stream);
+
+/*
+ * One whole round: draft -> schedule -> verify on one stream, with no host
+ * synchronisation in between (the scheduled lengths stay on the device).
+ * Arguments are the union of the three calls above; the intermediate outputs
+ * (draft_tokens, q_tok, q_stats, sched_len, K, tau_theta) are written too.
+ */
+dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                           const void* base_logits, const void* target_logits,
+                           const int32_t* anchor, const void* W1, const void* W2,
+                           const float* conf, const float* conf_lagged,
+                           const float* sps_table, int32_t n_table, int32_t mode,
+                           float temperature, uint64_t seed, int32_t* draft_tokens,
+                           float* q_tok, float* q_stats, int32_t* sched_len, int32_t* K,
+                           double* tau_theta, int32_t* out_tokens, int32_t* accepted_len,
+                           float* p_tok, void* workspace, size_t workspace_bytes,
+                           dspark_stream_t stream);
+
+/* Synchronises `stream`, then returns the workspace's sticky device status
+ * (DSPARK_OK if no device-side error was recorded). */
+dspark_status dspark_device_status(const void* workspace, dspark_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* dspark_status_string(dspark_status status);
+
+/* Number of kernel launches the most recent call of each entry point made on
+ * this thread (for launch accounting in benchmarks). */
+int32_t dspark_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,215 @@
+// Shared device/host helpers of the DSpark GB300 library: workspace layout,
+// status word, input loaders, the Philox4x64-10 uniform and block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <math.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// Columns per vocabulary chunk: the unit of the per-(row, chunk) softmax
+// partials that the sampling locate step scans.
+constexpr int kChunk = 64;
+
+inline __host__ __device__ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+inline __host__ __device__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Per-request pending draw of the verifier (residual or bonus).
+enum PendKind : int { kPendNone = 0, kPendResid = 1, kPendBonus = 2 };
+
+// Byte offsets of the workspace sections.
+struct WsLayout {
+  size_t status;   // u32[64]: [0] sticky status, [1..] counters
+  size_t dpart;    // float2 [R][n_chunks]   draft chunk partials (m, s) or (max, idx)
+  size_t rowstat;  // float4 [R][gamma+1]    target row stats (M, Z, argmax, unused)
+  size_t pend;     // int4   [R]             (kind, target row, prev token, accepted)
+  size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
+  size_t skey0, skey1, sidx0, sidx1;  // u32 [R*gamma] radix-sort ping-pong
+  size_t fx;       // u64 [R*gamma]         fixed-point prefix sums in sorted order
+  size_t total;
+};
+
+inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
+  WsLayout L;
+  const size_t nc = (size_t)ceil_div(V, kChunk);
+  const size_t n = (size_t)R * (size_t)gamma > 0 ? (size_t)R * (size_t)gamma : 1;
+  size_t o = 0;
+  L.status = o;  o = align256(o + 64 * sizeof(uint32_t));
+  L.dpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
+  L.rowstat = o; o = align256(o + (size_t)R * (gamma + 1) * sizeof(float4));
+  L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
+  L.rpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
+  L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));
+  L.skey1 = o;   o = align256(o + n * sizeof(uint32_t));
+  L.sidx0 = o;   o = align256(o + n * sizeof(uint32_t));
+  L.sidx1 = o;   o = align256(o + n * sizeof(uint32_t));
+  L.fx = o;      o = align256(o + n * sizeof(unsigned long long));
+  L.total = o;
+  return L;
+}
+
+template <class T>
+inline __host__ __device__ T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+// First device-side error wins; later ones are dropped (sticky word).
+__device__ __forceinline__ void set_status(uint32_t* status, int code) {
+  atomicCAS(status, 0u, (uint32_t)code);
+}
+
+// Element loaders: bf16 bit patterns or float32, returned as float (exact).
+__device__ __forceinline__ float ld_elem(const float* p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, size_t i) {
+  const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p) + i);
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of the 4x64
+// round function with the generator's published multipliers and Weyl key
+// increments; u = (2 * (w0 >> 12) + 1) * 2^-53 is an exact double in (0, 1).
+enum Purpose : uint64_t { kDraft = 0, kAccept = 1, kResid = 2, kBonus = 3 };
+
+__device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t r, uint64_t k, uint64_t purpose) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  uint64_t c0 = r, c1 = k, c2 = purpose, c3 = 0;
+  uint64_t k0 = seed, k1 = 0x44535041524B0000ull;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    k0 += W0; k1 += W1;
+  }
+  return (double)(2ull * (c0 >> 12) + 1ull) * 0x1p-53;
+}
+
+// ---------------------------------------------------------------------------
+// Warp / block reductions with a fixed combination order (deterministic).
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// (value, index) argmax with the lowest index on ties.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide reductions for blockDim.x a multiple of 32 (<= 1024); `sh` needs
+// 32 slots. All threads receive the result.
+__device__ __forceinline__ float block_max(float v, float* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  v = lane < nw ? sh[lane] : -INFINITY;
+  return warp_max(v);
+}
+__device__ __forceinline__ int block_min_i(int v, int* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_min_i(v);
+  __syncthreads();
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  v = lane < nw ? sh[lane] : 0x7fffffff;
+  return warp_min_i(v);
+}
+__device__ __forceinline__ int block_max_i(int v, int* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max_i(v);
+  __syncthreads();
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  v = lane < nw ? sh[lane] : -0x7fffffff;
+  return warp_max_i(v);
+}
+__device__ __forceinline__ void block_argmax(float& v, int& i, float* shv, int* shi) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  warp_argmax(v, i);
+  __syncthreads();
+  if (lane == 0) { shv[w] = v; shi[w] = i; }
+  __syncthreads();
+  v = lane < nw ? shv[lane] : -INFINITY;
+  i = lane < nw ? shi[lane] : 0x7fffffff;
+  warp_argmax(v, i);
+}
+// Exclusive scan of one double per thread (thread order); returns the total.
+// The exclusive value is read from the neighbouring lane's inclusive sum
+// rather than formed by subtraction.
+__device__ __forceinline__ double block_exscan_d(double v, double* sh, double& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  double x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  double ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = 0.0;
+  __syncthreads();
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    double s = lane < nw ? sh[lane] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) sh[lane] = s;
+  }
+  __syncthreads();
+  total = sh[nw - 1];
+  const double before_warp = w > 0 ? sh[w - 1] : 0.0;
+  const double res = before_warp + ex;
+  __syncthreads();
+  return res;
+}
+
+// Draft / target weight of one vocabulary entry relative to a chunk maximum,
+// fixed to explicit round-to-nearest operations so every kernel that forms it
+// (partials, locate, residual) produces identical bits:
+//   d = (base - m) + bias,  w = 2^(d * log2(e) / T).
+__device__ __forceinline__ float draft_weight(float base, float bias, float m, float kT) {
+  const float d = __fadd_rn(__fsub_rn(base, m), bias);
+  return exp2f(__fmul_rn(d, kT));
+}
+__device__ __forceinline__ float draft_logit(float base, float bias) { return __fadd_rn(base, bias); }
+
+}  // namespace dspark

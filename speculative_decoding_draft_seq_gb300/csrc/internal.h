@@ -1,0 +1,62 @@
+// Internal launch interface between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+struct DraftArgs {
+  int R, gamma, V, rank, dtype;
+  const void* base;
+  const int32_t* anchor;
+  const void* W1;
+  const void* W2;
+  float temperature;
+  uint64_t seed;
+  int32_t* tokens;
+  float* q_tok;
+  float* q_stats;
+  void* ws;
+};
+
+struct ScheduleArgs {
+  int R, gamma;
+  const float* conf;
+  const float* conf_lagged;
+  const float* sps;
+  int n_table, mode;
+  int32_t* sched_len;
+  int32_t* K;
+  double* tau_theta;
+  void* ws;
+};
+
+struct VerifyArgs {
+  int R, gamma, V, rank, dtype;
+  const void* target;
+  const void* base;
+  const int32_t* anchor;
+  const void* W1;
+  const void* W2;
+  const int32_t* tokens;
+  const float* q_tok;
+  const float* q_stats;
+  const int32_t* sched_len;
+  float temperature;
+  uint64_t seed;
+  int32_t* out_tokens;
+  int32_t* accepted_len;
+  float* p_tok;
+  void* ws;
+};
+
+// Each launcher enqueues its kernels on `s`, adds the number of kernel
+// launches to `launches`, and returns cudaGetLastError().
+cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches);
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches);
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches);
+
+}  // namespace dspark

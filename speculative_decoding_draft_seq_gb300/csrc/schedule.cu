@@ -1,0 +1,285 @@
+// Hardware-aware prefix scheduler ("DSpark: Aceleração da inferência de LLM com
+// speculative decoding [pdf]" (GeekNews), "Verificação com agendamento por
+// confiança": cumulative prefix survival a_{r,j} = prod c_{r,i}; all R x gamma
+// candidates merged by a in descending order and admitted greedily against the
+// steps-per-second table SPS(B), stopping at the first admission that lowers
+// Theta = tau * SPS(B); production variant in "Aplicação prática do scheduler":
+// K from the confidences of two steps earlier by an unconstrained search, then
+// the top K of the current ranking).
+//
+// One CTA of 1024 threads (the problem is at most 65536 keys and latency
+// bound): survival products per request in float32, a stable LSD radix sort of
+// 32-bit keys (4-bit digits, per-thread contiguous segments, counts scanned in
+// digit-major order) with the flat candidate index as payload, an exact
+// fixed-point (2^-40) inclusive scan of the sorted survivals, and the
+// Theta_i comparisons in float64 with the operation order fixed by the C ABI.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+constexpr int kSchedThreads = 1024;
+constexpr int kDigits = 16;
+
+// Exclusive scan of one unsigned 64-bit value per thread; returns the total.
+__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v,
+                                                               unsigned long long* sh,
+                                                               unsigned long long& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  unsigned long long ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = 0;
+  __syncthreads();
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long s = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) sh[lane] = s;
+  }
+  __syncthreads();
+  total = sh[nw - 1];
+  const unsigned long long res = (w > 0 ? sh[w - 1] : 0ull) + ex;
+  __syncthreads();
+  return res;
+}
+
+// a in [0, 1] -> ascending sort key (descending a); bits of +0.0 .. 1.0.
+__device__ __forceinline__ uint32_t survival_key(float a) { return 0x3F800000u - __float_as_uint(a); }
+__device__ __forceinline__ float key_survival(uint32_t key) { return __uint_as_float(0x3F800000u - key); }
+
+__device__ __forceinline__ unsigned long long fixed_point(float a) {
+  return __double2ull_rz(__dadd_rn(__dmul_rn((double)a, 1099511627776.0), 0.5));
+}
+
+__device__ __forceinline__ double theta_of(int R, unsigned long long S, float sps) {
+  const double tau = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
+  return __dmul_rn(tau, (double)sps);
+}
+
+// Survival keys of one confidence matrix; flags non-finite entries.
+__device__ void build_keys(const float* conf, int R, int gamma, uint32_t* key, uint32_t* idx,
+                           uint32_t* status) {
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    float acc = 1.f;
+    for (int j = 0; j < gamma; ++j) {
+      float c = conf[(size_t)r * gamma + j];
+      if (!isfinite(c)) {
+        set_status(status, DSPARK_ERR_NONFINITE);
+        c = 0.f;
+      }
+      c = c > 0.f ? fminf(c, 1.f) : 0.f;
+      acc = __fmul_rn(acc, c);
+      key[(size_t)r * gamma + j] = survival_key(acc);
+      idx[(size_t)r * gamma + j] = (uint32_t)(r * gamma + j);
+    }
+  }
+  __syncthreads();
+}
+
+// Stable LSD radix sort of (key, idx), 8 passes of 4 bits; result in key0/idx0.
+__device__ void radix_sort(uint32_t* key0, uint32_t* idx0, uint32_t* key1, uint32_t* idx1, int n,
+                           uint32_t* cnt, unsigned long long* shu) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int seg = ceil_div(n, T);
+  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
+  uint32_t *kin = key0, *iin = idx0, *kout = key1, *iout = idx1;
+  for (int shift = 0; shift < 32; shift += 4) {
+    for (int d = 0; d < kDigits; ++d) cnt[d * T + tid] = 0;
+    for (int i = s0; i < s1; ++i) cnt[((kin[i] >> shift) & 15u) * T + tid] += 1;
+    __syncthreads();
+    uint32_t loc[kDigits];
+    unsigned long long sum = 0;
+#pragma unroll
+    for (int j = 0; j < kDigits; ++j) {
+      loc[j] = cnt[kDigits * tid + j];
+      sum += loc[j];
+    }
+    unsigned long long tot;
+    unsigned long long run = block_exscan_u64(sum, shu, tot);
+#pragma unroll
+    for (int j = 0; j < kDigits; ++j) {
+      cnt[kDigits * tid + j] = (uint32_t)run;
+      run += loc[j];
+    }
+    __syncthreads();
+    for (int i = s0; i < s1; ++i) {
+      const uint32_t k = kin[i];
+      const uint32_t slot = ((k >> shift) & 15u) * T + tid;
+      const uint32_t pos = cnt[slot];
+      cnt[slot] = pos + 1;
+      kout[pos] = k;
+      iout[pos] = iin[i];
+    }
+    __syncthreads();
+    uint32_t* t;
+    t = kin; kin = kout; kout = t;
+    t = iin; iin = iout; iout = t;
+  }
+}
+
+// fx[i] = sum of fixed_point(a) over sorted positions 0..i.
+__device__ void fixed_prefix(const uint32_t* key, int n, unsigned long long* fx, unsigned long long* shu) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int seg = ceil_div(n, T);
+  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
+  unsigned long long loc = 0;
+  for (int i = s0; i < s1; ++i) loc += fixed_point(key_survival(key[i]));
+  unsigned long long tot;
+  unsigned long long run = block_exscan_u64(loc, shu, tot);
+  for (int i = s0; i < s1; ++i) {
+    run += fixed_point(key_survival(key[i]));
+    fx[i] = run;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
+    int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
+    const float* __restrict__ sps, int n_table, int mode, int32_t* __restrict__ L,
+    int32_t* __restrict__ Kout, double* __restrict__ tau_theta, uint32_t* key0, uint32_t* key1,
+    uint32_t* idx0, uint32_t* idx1, unsigned long long* fx, uint32_t* status) {
+  extern __shared__ uint32_t cnt[];  // kDigits * blockDim.x
+  __shared__ unsigned long long shu[32];
+  __shared__ int shi[32];
+  __shared__ double shd[32];
+  __shared__ int sBad;
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int n = R * gamma;
+
+  if (tid == 0) sBad = 0;
+  __syncthreads();
+  for (int i = tid; i < n_table; i += T)
+    if (!isfinite(sps[i])) sBad = 1;
+  for (int r = tid; r < R; r += T) L[r] = (mode == DSPARK_SCHED_ALL) ? gamma : 0;
+  __syncthreads();
+  if (sBad) {
+    if (tid == 0) {
+      set_status(status, DSPARK_ERR_NONFINITE);
+      *Kout = 0;
+      tau_theta[0] = (double)R;
+      tau_theta[1] = 0.0;
+    }
+    for (int r = tid; r < R; r += T) L[r] = 0;
+    return;
+  }
+
+  if (mode == DSPARK_SCHED_ALL) {
+    build_keys(conf, R, gamma, key0, idx0, status);
+    unsigned long long loc = 0;
+    for (int i = tid; i < n; i += T) loc += fixed_point(key_survival(key0[i]));
+    unsigned long long tot;
+    block_exscan_u64(loc, shu, tot);
+    if (tid == 0) {
+      *Kout = n;
+      tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(tot), 0x1p-40));
+      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, tot, sps[R + n - 1]) : 0.0;
+    }
+    return;
+  }
+
+  if (R > n_table) {
+    if (tid == 0) {
+      *Kout = 0;
+      tau_theta[0] = (double)R;
+      tau_theta[1] = 0.0;
+    }
+    return;
+  }
+
+  int K = 0;
+  if (mode == DSPARK_SCHED_LAGGED) {
+    build_keys(conf_lag, R, gamma, key0, idx0, status);
+    radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
+    fixed_prefix(key0, n, fx, shu);
+    const int imax = min(n, n_table - R);
+    // smallest argmax of Theta_i, i = 0..imax
+    double best = -INFINITY;
+    int besti = 0x7fffffff;
+    for (int i = tid; i <= imax; i += T) {
+      const unsigned long long S = i ? fx[i - 1] : 0ull;
+      const double th = theta_of(R, S, sps[R + i - 1]);
+      if (th > best || (th == best && i < besti)) { best = th; besti = i; }
+    }
+    // block (value, index) argmax in float64
+    const int lane = tid & 31, w = tid >> 5, nw = T >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+      if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
+    }
+    __syncthreads();
+    if (lane == 0) { shd[w] = best; shi[w] = besti; }
+    __syncthreads();
+    best = lane < nw ? shd[lane] : -INFINITY;
+    besti = lane < nw ? shi[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+      if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
+    }
+    K = besti;
+    __syncthreads();
+  }
+
+  build_keys(conf, R, gamma, key0, idx0, status);
+  radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
+  fixed_prefix(key0, n, fx, shu);
+
+  if (mode == DSPARK_SCHED_CAUSAL) {
+    const int seg = ceil_div(n, T);
+    const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
+    int stop = 0x7fffffff;
+    for (int i = s0; i < s1; ++i) {
+      const int B = R + i + 1;
+      bool st = B > n_table;
+      if (!st) {
+        const double th_next = theta_of(R, fx[i], sps[B - 1]);
+        const double th_prev = theta_of(R, i ? fx[i - 1] : 0ull, sps[B - 2]);
+        st = th_next < th_prev;
+      }
+      if (st) { stop = i; break; }
+    }
+    K = block_min_i(stop, shi);
+    if (K == 0x7fffffff) K = n;
+  }
+
+  for (int i = tid; i < K; i += T) atomicAdd(&L[idx0[i] / (uint32_t)gamma], 1);
+  if (tid == 0) {
+    const unsigned long long S = K ? fx[K - 1] : 0ull;
+    *Kout = K;
+    tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
+    tau_theta[1] = theta_of(R, S, sps[R + K - 1]);
+  }
+}
+
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches) {
+  const WsLayout L = ws_layout(a.R, a.gamma, 1);
+  void* ws = a.ws;
+  const size_t smem = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  schedule_kernel<<<1, kSchedThreads, smem, s>>>(
+      a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table, a.mode, a.sched_len, a.K, a.tau_theta,
+      ws_at<uint32_t>(ws, L.skey0), ws_at<uint32_t>(ws, L.skey1), ws_at<uint32_t>(ws, L.sidx0),
+      ws_at<uint32_t>(ws, L.sidx1), ws_at<unsigned long long>(ws, L.fx), ws_at<uint32_t>(ws, L.status));
+  launches += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,363 @@
+// Lossless speculative-sampling verification ("DSpark: Aceleração da inferência
+// de LLM com speculative decoding [pdf]" (GeekNews), "Definição do problema":
+// the target checks the drafted block in one pass and rejection sampling keeps
+// the longest prefix consistent with the target distribution; decoding-cycle
+// paragraph: E and F accepted, G rejected, corrected token G* emitted).
+//
+// Four launches:
+//   verify_stats   one CTA per scheduled target row (r, k <= L_r): streams the
+//                  row once with 128-bit loads, online max / sum of
+//                  2^((t - m) log2(e) / T) per thread, float64 block combine;
+//                  writes (M, Z, argmax) and p_tok = P_k(x_{k+1}).
+//   verify_chain   one thread per request: ratio tests u < p / q in order;
+//                  first rejection j = A + 1 -> residual draw, otherwise the
+//                  bonus draw from row L_r = A. Both use target row A.
+//   resid_partials per (64-column chunk, 32 requests): residual weights
+//                  max(0, P - Q) (Q recomputed with the Markov bias of the
+//                  rejected position) or bonus weights P, chunk sums.
+//   resid_locate   one CTA per request: float64 scan of chunk sums, inverse
+//                  CDF, recompute of the crossing chunk, emitted token.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+constexpr int kStatThreads = 512;
+constexpr int kRRows = 32;
+constexpr int kRKBlock = 32;
+
+template <class Tin>
+__device__ __forceinline__ float bias_dot_v(const Tin* W1, const Tin* W2, int prev, int rank, int V, int v) {
+  float acc = 0.f;
+  const size_t w1row = (size_t)prev * rank;
+  for (int i = 0; i < rank; ++i) acc = __fmaf_rn(ld_elem(W1, w1row + i), ld_elem(W2, (size_t)i * V + v), acc);
+  return acc;
+}
+
+__device__ __forceinline__ float target_weight(float t, float m, float kT) {
+  return exp2f(__fmul_rn(__fsub_rn(t, m), kT));
+}
+
+struct OnlineStat {
+  float m = -INFINITY, s = 0.f, am = -INFINITY;
+  int ai = 0x7fffffff;
+  __device__ __forceinline__ void add8(const float (&t)[8], int v0, float kT, bool greedy) {
+    float gm = t[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) gm = fmaxf(gm, t[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (t[i] > am) { am = t[i]; ai = v0 + i; }  // strict: keeps the first index of a tie
+    if (greedy) return;
+    if (gm > m) {
+      s = __fmul_rn(s, target_weight(m, gm, kT));
+      m = gm;
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part += target_weight(t[i], m, kT);
+    s += part;
+  }
+  __device__ __forceinline__ void add1(float t, int v, float kT, bool greedy) {
+    if (t > am) { am = t; ai = v; }
+    if (greedy) return;
+    if (t > m) {
+      s = __fmul_rn(s, target_weight(m, t, kT));
+      m = t;
+    }
+    s += target_weight(t, m, kT);
+  }
+};
+
+template <class Tin>
+__global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
+    int R, int gamma, int V, const Tin* __restrict__ target, const int32_t* __restrict__ tokens,
+    const int32_t* __restrict__ sched_len, float kT, int greedy, float4* __restrict__ rowstat,
+    float* __restrict__ p_tok, uint32_t* status) {
+  __shared__ float shf[32];
+  __shared__ int shi[32];
+  __shared__ double shd[32];
+  const int r = blockIdx.x, k = blockIdx.y, tid = threadIdx.x;
+  const int L = min(max(sched_len[r], 0), gamma);
+  if (k > L) return;
+  const size_t row = ((size_t)r * (gamma + 1) + k) * V;
+  OnlineStat st;
+  // per-thread spans are interleaved in 8-element groups (coalesced 16-byte loads)
+  if (sizeof(Tin) == 2 && (V & 7) == 0) {
+    const uint4* p = reinterpret_cast<const uint4*>(target + row);
+    const int ng = V >> 3;
+    for (int g = tid; g < ng; g += blockDim.x) {
+      const uint4 q = __ldg(p + g);
+      float t[8];
+      t[0] = bf16_bits_to_float(q.x & 0xffffu); t[1] = bf16_bits_to_float(q.x >> 16);
+      t[2] = bf16_bits_to_float(q.y & 0xffffu); t[3] = bf16_bits_to_float(q.y >> 16);
+      t[4] = bf16_bits_to_float(q.z & 0xffffu); t[5] = bf16_bits_to_float(q.z >> 16);
+      t[6] = bf16_bits_to_float(q.w & 0xffffu); t[7] = bf16_bits_to_float(q.w >> 16);
+      st.add8(t, g * 8, kT, greedy);
+    }
+  } else {
+    for (int v = tid; v < V; v += blockDim.x) st.add1(ld_elem(target, row + v), v, kT, greedy);
+  }
+  float am = st.am;
+  int ai = st.ai;
+  block_argmax(am, ai, shf, shi);
+  float M = 0.f;
+  double Z = 1.0;
+  if (!greedy) {
+    M = block_max(st.m, shf);
+    const double contrib = st.s > 0.f ? (double)st.s * (double)target_weight(st.m, M, kT) : 0.0;
+    block_exscan_d(contrib, shd, Z);
+  }
+  if (tid == 0) {
+    rowstat[(size_t)r * (gamma + 1) + k] = make_float4(M, (float)Z, __int_as_float(ai), 0.f);
+    if (k < L) {
+      int x = tokens[(size_t)r * gamma + k];
+      if (x < 0 || x >= V) { set_status(status, DSPARK_ERR_RANGE); x = min(max(x, 0), V - 1); }
+      float p;
+      if (greedy) p = (x == ai) ? 1.f : 0.f;
+      else p = (float)((double)target_weight(ld_elem(target, row + x), M, kT) / Z);
+      p_tok[(size_t)r * gamma + k] = p;
+    }
+  }
+}
+
+__global__ void verify_chain_kernel(int R, int gamma, const int32_t* __restrict__ tokens,
+                                    const int32_t* __restrict__ anchor, const float* __restrict__ q_tok,
+                                    const int32_t* __restrict__ sched_len, uint64_t seed, int greedy,
+                                    const float4* __restrict__ rowstat, float* __restrict__ p_tok,
+                                    int32_t* __restrict__ out, int32_t* __restrict__ acc_len,
+                                    int4* __restrict__ pend) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const int L = min(max(sched_len[r], 0), gamma);
+  int A = L;
+  for (int k = 1; k <= L; ++k) {
+    const float p = p_tok[(size_t)r * gamma + k - 1];
+    const float q = q_tok[(size_t)r * gamma + k - 1];
+    const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)k, kAccept);
+    const bool ok = (q <= 0.f) || (u < (double)p / (double)q);
+    if (!ok) { A = k - 1; break; }
+  }
+  acc_len[r] = A;
+  for (int k = 0; k < A; ++k) out[(size_t)r * (gamma + 1) + k] = tokens[(size_t)r * gamma + k];
+  for (int k = A + 1; k <= gamma; ++k) out[(size_t)r * (gamma + 1) + k] = -1;
+  for (int k = L; k < gamma; ++k) p_tok[(size_t)r * gamma + k] = 0.f;
+  const int prev = A ? tokens[(size_t)r * gamma + A - 1] : anchor[r];
+  if (greedy) {
+    out[(size_t)r * (gamma + 1) + A] = __float_as_int(rowstat[(size_t)r * (gamma + 1) + A].z);
+    pend[r] = make_int4(kPendNone, A, prev, A);
+  } else {
+    pend[r] = make_int4(A < L ? kPendResid : kPendBonus, A, prev, A);
+  }
+}
+
+// Residual (or bonus) weight of one entry, with explicit rounding so the
+// partials and the locate recompute agree bit for bit.
+__device__ __forceinline__ float resid_weight(int kind, float t, float MP, float ZP, float b, float bias,
+                                              float MQ, float ZQ, float kT) {
+  const float P = __fdiv_rn(target_weight(t, MP, kT), ZP);
+  if (kind == kPendBonus) return P;
+  const float Q = __fdiv_rn(draft_weight(b, bias, MQ, kT), ZQ);
+  return fmaxf(0.f, __fsub_rn(P, Q));
+}
+
+template <class Tin>
+__global__ void __launch_bounds__(256) resid_partials_kernel(
+    int R, int gamma, int V, int rank, const Tin* __restrict__ target, const Tin* __restrict__ base,
+    const Tin* __restrict__ W1, const Tin* __restrict__ W2, const float* __restrict__ q_stats,
+    const float4* __restrict__ rowstat, const int4* __restrict__ pend, float kT,
+    float2* __restrict__ rpart) {
+  __shared__ float sW1[kRRows][kRKBlock + 1];
+  __shared__ float sW2[kRKBlock][kChunk];
+  __shared__ int4 sPend[kRRows];
+  __shared__ float sRed[kRRows][2][2];
+  __shared__ int sAny;
+  const int nc = ceil_div(V, kChunk);
+  const int chunk = blockIdx.x, row0 = blockIdx.y * kRRows;
+  const int tid = threadIdx.x, col = tid & 63, rg = tid >> 6, half = (tid >> 5) & 1;
+  const int v = chunk * kChunk + col;
+  if (tid == 0) sAny = 0;
+  __syncthreads();
+  if (tid < kRRows) {
+    const int r = row0 + tid;
+    int4 pd = r < R ? pend[r] : make_int4(kPendNone, 0, 0, 0);
+    sPend[tid] = pd;
+    if (pd.x != kPendNone) atomicOr(&sAny, 1);
+  }
+  __syncthreads();
+  if (!sAny) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int kb = 0; kb < rank; kb += kRKBlock) {
+    for (int i = tid; i < kRRows * kRKBlock; i += 256) {
+      const int rr = i / kRKBlock, kk = i % kRKBlock;
+      sW1[rr][kk] = (kb + kk < rank) ? ld_elem(W1, (size_t)sPend[rr].z * rank + kb + kk) : 0.f;
+    }
+    for (int i = tid; i < kRKBlock * kChunk; i += 256) {
+      const int kk = i / kChunk, cc = i % kChunk, vv = chunk * kChunk + cc;
+      sW2[kk][cc] = (kb + kk < rank && vv < V) ? ld_elem(W2, (size_t)(kb + kk) * V + vv) : 0.f;
+    }
+    __syncthreads();
+    const int kmax = min(kRKBlock, rank - kb);
+    for (int kk = 0; kk < kmax; ++kk) {
+      const float w2 = sW2[kk][col];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(sW1[rg * 8 + i][kk], w2, acc[i]);
+    }
+    __syncthreads();
+  }
+#pragma unroll 1
+  for (int i = 0; i < 8; ++i) {
+    const int rl = rg * 8 + i, r = row0 + rl;
+    const int4 pd = sPend[rl];
+    const bool valid = (r < R) && (v < V) && pd.x != kPendNone;
+    float w = 0.f, pw = 0.f;
+    if (valid) {
+      const int A = pd.y;
+      const float4 rs = rowstat[(size_t)r * (gamma + 1) + A];
+      const float t = ld_elem(target, ((size_t)r * (gamma + 1) + A) * V + v);
+      pw = __fdiv_rn(target_weight(t, rs.x, kT), rs.y);
+      if (pd.x == kPendBonus) {
+        w = pw;
+      } else {
+        const float b = ld_elem(base, ((size_t)r * gamma + A) * V + v);
+        const float MQ = q_stats[2 * ((size_t)r * gamma + A)], ZQ = q_stats[2 * ((size_t)r * gamma + A) + 1];
+        w = resid_weight(kPendResid, t, rs.x, rs.y, b, acc[i], MQ, ZQ, kT);
+      }
+    }
+    const float sw = warp_sum(w), sp = warp_sum(pw);
+    if ((tid & 31) == 0) { sRed[rl][half][0] = sw; sRed[rl][half][1] = sp; }
+    __syncthreads();
+    if (col == 0 && r < R && pd.x != kPendNone)
+      rpart[(size_t)r * nc + chunk] = make_float2(sRed[rl][0][0] + sRed[rl][1][0], sRed[rl][0][1] + sRed[rl][1][1]);
+    __syncthreads();
+  }
+}
+
+template <class Tin>
+__global__ void __launch_bounds__(256) resid_locate_kernel(
+    int R, int gamma, int V, int rank, const Tin* __restrict__ target, const Tin* __restrict__ base,
+    const Tin* __restrict__ W1, const Tin* __restrict__ W2, const float* __restrict__ q_stats,
+    const float4* __restrict__ rowstat, const int4* __restrict__ pend, float kT, uint64_t seed,
+    const float2* __restrict__ rpart, int32_t* __restrict__ out) {
+  __shared__ int shi[32];
+  __shared__ double shd[32];
+  __shared__ float sW[kChunk];
+  __shared__ double sExcl;
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int4 pd = pend[r];
+  if (pd.x == kPendNone) return;
+  const int nc = ceil_div(V, kChunk);
+  const float2* pr = rpart + (size_t)r * nc;
+  const int A = pd.y;
+  const int seg = ceil_div(nc, blockDim.x);
+  const int c0 = min(nc, tid * seg), c1 = min(nc, c0 + seg);
+
+  double loc_res = 0.0;
+  for (int c = c0; c < c1; ++c) loc_res += (double)pr[c].x;
+  double W;
+  double excl = block_exscan_d(loc_res, shd, W);
+  int use_p = 0;
+  if (!(W > 0.0)) {  // empty residual under rounding: draw from P instead
+    use_p = 1;
+    double loc_p = 0.0;
+    for (int c = c0; c < c1; ++c) loc_p += (double)pr[c].y;
+    excl = block_exscan_d(loc_p, shd, W);
+  }
+  const uint64_t purpose = pd.x == kPendResid ? kResid : kBonus;
+  const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)(A + 1), purpose);
+  const double target_v = u * W;
+
+  int found = 0x7fffffff, last_pos = -1;
+  double run = excl, found_excl = 0.0;
+  for (int c = c0; c < c1; ++c) {
+    const double f = (double)(use_p ? pr[c].y : pr[c].x);
+    if (f > 0.0) last_pos = c;
+    if (found == 0x7fffffff) {
+      if (run + f > target_v) { found = c; found_excl = run; }
+      run += f;
+    }
+  }
+  int cstar = block_min_i(found, shi);
+  if (found == cstar && cstar != 0x7fffffff) sExcl = found_excl;
+  bool fallback = false;
+  if (cstar == 0x7fffffff) {
+    cstar = max(0, block_max_i(last_pos, shi));
+    fallback = true;
+  }
+  __syncthreads();
+  const int kind = use_p ? kPendBonus : pd.x;
+  const float4 rs = rowstat[(size_t)r * (gamma + 1) + A];
+  if (tid < kChunk) {
+    const int v = cstar * kChunk + tid;
+    float w = 0.f;
+    if (v < V) {
+      const float t = ld_elem(target, ((size_t)r * (gamma + 1) + A) * V + v);
+      if (kind == kPendBonus) {
+        w = resid_weight(kPendBonus, t, rs.x, rs.y, 0.f, 0.f, 0.f, 1.f, kT);
+      } else {
+        const float b = ld_elem(base, ((size_t)r * gamma + A) * V + v);
+        const float MQ = q_stats[2 * ((size_t)r * gamma + A)], ZQ = q_stats[2 * ((size_t)r * gamma + A) + 1];
+        w = resid_weight(kPendResid, t, rs.x, rs.y, b, bias_dot_v(W1, W2, pd.z, rank, V, v), MQ, ZQ, kT);
+      }
+    }
+    sW[tid] = w;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int xc = -1;
+    if (!fallback) {
+      double run2 = sExcl;
+      for (int c = 0; c < kChunk; ++c) {
+        run2 += (double)sW[c];
+        if (run2 > target_v) { xc = c; break; }
+      }
+    }
+    if (xc < 0) {
+      for (int c = kChunk - 1; c >= 0; --c)
+        if (sW[c] > 0.f) { xc = c; break; }
+      if (xc < 0) xc = 0;
+    }
+    out[(size_t)r * (gamma + 1) + A] = min(cstar * kChunk + xc, V - 1);
+  }
+}
+
+template <class Tin>
+static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& launches) {
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  void* ws = a.ws;
+  uint32_t* status = ws_at<uint32_t>(ws, L.status);
+  float4* rowstat = ws_at<float4>(ws, L.rowstat);
+  int4* pend = ws_at<int4>(ws, L.pend);
+  float2* rpart = ws_at<float2>(ws, L.rpart);
+  const int greedy = a.temperature == 0.f;
+  const float kT = greedy ? 0.f : (float)(1.4426950408889634 / (double)a.temperature);
+  const Tin* target = static_cast<const Tin*>(a.target);
+  const Tin* base = static_cast<const Tin*>(a.base);
+  const Tin* W1 = static_cast<const Tin*>(a.W1);
+  const Tin* W2 = static_cast<const Tin*>(a.W2);
+  verify_stats_kernel<Tin><<<dim3(a.R, a.gamma + 1), kStatThreads, 0, s>>>(
+      a.R, a.gamma, a.V, target, a.tokens, a.sched_len, kT, greedy, rowstat, a.p_tok, status);
+  verify_chain_kernel<<<ceil_div(a.R, 128), 128, 0, s>>>(a.R, a.gamma, a.tokens, a.anchor, a.q_tok,
+                                                          a.sched_len, a.seed, greedy, rowstat, a.p_tok,
+                                                          a.out_tokens, a.accepted_len, pend);
+  launches += 2;
+  if (!greedy) {
+    const int nc = ceil_div(a.V, kChunk);
+    resid_partials_kernel<Tin><<<dim3(nc, ceil_div(a.R, kRRows)), 256, 0, s>>>(
+        a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats, rowstat, pend, kT, rpart);
+    resid_locate_kernel<Tin><<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, target, base, W1, W2,
+                                                 a.q_stats, rowstat, pend, kT, a.seed, rpart,
+                                                 a.out_tokens);
+    launches += 2;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches) {
+  if (a.dtype == DSPARK_BF16) return launch_verify_t<__nv_bfloat16>(a, s, launches);
+  return launch_verify_t<float>(a, s, launches);
+}
+
+}  // namespace dspark

@@ -1,0 +1,163 @@
+"""Python binding of the DSpark C-ABI library (libdspark.so).
+
+Argument marshalling only: every step of the round runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (device memory and streams are
+PyTorch's); the binding passes their data pointers and the current stream's
+handle to the C entry points declared in include/dspark.h. If the library is
+missing the import fails: there is no fallback implementation.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdspark.so")
+
+OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_RANGE = range(7)
+FP32, BF16 = 0, 1
+CAUSAL, LAGGED, ALL = 0, 1, 2
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    i32, u64, f32, vp, sz = ctypes.c_int32, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    lib.dspark_workspace_bytes.restype = sz
+    lib.dspark_workspace_bytes.argtypes = [i32] * 6
+    lib.dspark_workspace_init.restype = i32
+    lib.dspark_workspace_init.argtypes = [vp, sz, vp]
+    lib.dspark_draft_sequential.restype = i32
+    lib.dspark_draft_sequential.argtypes = [i32] * 5 + [vp] * 4 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
+    lib.dspark_schedule.restype = i32
+    lib.dspark_schedule.argtypes = [i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.dspark_verify.restype = i32
+    lib.dspark_verify.argtypes = [i32] * 5 + [vp] * 9 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
+    lib.dspark_round.restype = i32
+    lib.dspark_round.argtypes = ([i32] * 5 + [vp] * 5 + [vp, vp, vp, i32, i32, f32, u64] +
+                                 [vp] * 9 + [vp, sz, vp])
+    lib.dspark_device_status.restype = i32
+    lib.dspark_device_status.argtypes = [vp, vp]
+    lib.dspark_status_string.restype = ctypes.c_char_p
+    lib.dspark_status_string.argtypes = [i32]
+    lib.dspark_last_launch_count.restype = i32
+    lib.dspark_last_launch_count.argtypes = []
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status):
+    return lib.dspark_status_string(int(status)).decode()
+
+
+def last_launch_count():
+    return int(lib.dspark_last_launch_count())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"logits/weights must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check(status, where):
+    if status != OK:
+        raise DSparkError(status, where)
+
+
+def workspace_bytes(R, gamma, V, rank, dtype, n_table):
+    return int(lib.dspark_workspace_bytes(R, gamma, V, rank, dtype, n_table))
+
+
+def new_workspace(R, gamma, V, rank, dtype, n_table, device="cuda", stream=None):
+    """Allocates (with PyTorch) and clears a workspace for these sizes."""
+    n = workspace_bytes(R, gamma, V, rank, dtype, n_table)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    _check(lib.dspark_workspace_init(_ptr(ws), n, _stream(stream)), "dspark_workspace_init")
+    return ws
+
+
+def draft_sequential(base, anchor, W1, W2, temperature, seed, tokens, q_tok, q_stats, ws, stream=None):
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_draft_sequential(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor),
+                                       _ptr(W1), _ptr(W2), float(temperature), int(seed), _ptr(tokens),
+                                       _ptr(q_tok), _ptr(q_stats), _ptr(ws), ws.numel(), _stream(stream)),
+           "dspark_draft_sequential")
+
+
+def schedule(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, ws, stream=None):
+    R, gamma = conf.shape
+    _check(lib.dspark_schedule(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(), int(mode),
+                               _ptr(sched_len), _ptr(K), _ptr(tau_theta), _ptr(ws), ws.numel(),
+                               _stream(stream)), "dspark_schedule")
+
+
+def verify(target, base, anchor, W1, W2, tokens, q_tok, q_stats, sched_len, temperature, seed,
+           out_tokens, accepted_len, p_tok, ws, stream=None):
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_verify(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base), _ptr(anchor),
+                             _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(sched_len),
+                             float(temperature), int(seed), _ptr(out_tokens), _ptr(accepted_len),
+                             _ptr(p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_verify")
+
+
+def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,
+           stream=None):
+    """One whole round; `out` is a RoundOutputs holding the output tensors."""
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_round(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target), _ptr(anchor),
+                            _ptr(W1), _ptr(W2), _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(),
+                            int(mode), float(temperature), int(seed), _ptr(out.tokens), _ptr(out.q_tok),
+                            _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K), _ptr(out.tau_theta),
+                            _ptr(out.out_tokens), _ptr(out.accepted_len), _ptr(out.p_tok), _ptr(ws),
+                            ws.numel(), _stream(stream)), "dspark_round")
+
+
+def device_status(ws, stream=None):
+    return int(lib.dspark_device_status(_ptr(ws), _stream(stream)))
+
+
+class RoundOutputs:
+    """Device output tensors of one round for R requests and block length gamma."""
+
+    def __init__(self, R, gamma, device="cuda"):
+        i32, f32 = torch.int32, torch.float32
+        self.tokens = torch.zeros((R, gamma), dtype=i32, device=device)
+        self.q_tok = torch.zeros((R, gamma), dtype=f32, device=device)
+        self.q_stats = torch.zeros((R, gamma, 2), dtype=f32, device=device)
+        self.sched_len = torch.zeros((R,), dtype=i32, device=device)
+        self.K = torch.zeros((1,), dtype=i32, device=device)
+        self.tau_theta = torch.zeros((2,), dtype=torch.float64, device=device)
+        self.out_tokens = torch.zeros((R, gamma + 1), dtype=i32, device=device)
+        self.accepted_len = torch.zeros((R,), dtype=i32, device=device)
+        self.p_tok = torch.zeros((R, gamma), dtype=f32, device=device)
+
+    def host(self):
+        return {k: v.cpu().numpy() for k, v in vars(self).items()}

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the oracle.
+
+Small cases compare every request; the full-size workloads run the whole round
+on the device in the configuration the benchmark times and compare sampled
+requests (the oracle drafts and verifies them one by one; the schedule is
+always compared in full).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_harness import compare, device_inputs, gpu_round, oracle_round
+    from speculative_decoding_draft_seq_gb300 import dspark
+
+
+def _full(cfg):
+    g = gpu_round(cfg)
+    o = oracle_round(cfg, list(range(cfg.R)))
+    return compare(cfg, g, o, list(range(cfg.R))), g, o
+
+
+RAGGED_BF16 = W.Workload("ragged_bf16", R=40, gamma=5, V=1000, rank=48, dtype="bf16", T=0.9,
+                         mode=W.CAUSAL, seed=2001, base_sd=1.5, w_sd=0.05, target_sd=(0.5,),
+                         conf_law="decreasing", table="concave", n_table=240)
+RAGGED_FP32 = W.Workload("ragged_fp32", R=37, gamma=3, V=130, rank=5, dtype="fp32", T=1.3,
+                         mode=W.CAUSAL, seed=2002, base_sd=1.0, zipf=0.0, w_sd=0.4,
+                         target_sd=(0.6,), conf_law="uniform", table="concave", n_table=160)
+TC_SHAPE = W.Workload("tc_shape", R=150, gamma=4, V=3000, rank=64, dtype="bf16", T=1.0,
+                      mode=W.CAUSAL, seed=2003, base_sd=1.5, w_sd=0.05, target_sd=(0.45,),
+                      conf_law="decreasing", table="concave", n_table=150 * 5)
+
+
+@pytest.mark.parametrize("cfg", [W.CONFIGS["tiny"], W.with_(W.CONFIGS["tiny"], T=0.0),
+                                 RAGGED_BF16, W.with_(RAGGED_BF16, T=0.0), RAGGED_FP32,
+                                 TC_SHAPE, W.with_(TC_SHAPE, T=0.0)],
+                         ids=["tiny", "tiny_greedy", "ragged_bf16", "ragged_bf16_greedy",
+                              "ragged_fp32", "tc_shape", "tc_shape_greedy"])
+def test_round_parity_small(cfg):
+    rep, g, _ = _full(cfg)
+    assert rep["positions"] > 0
+    assert g["launches"] > 0
+
+
+@pytest.mark.parametrize("mode", [W.ALL, W.LAGGED])
+def test_round_parity_modes(mode):
+    cfg = W.with_(RAGGED_BF16, mode=mode, conf_law="beta_mixed", table="step", n_table=200)
+    _full(cfg)
+
+
+def test_small_vocab_config():
+    cfg = W.CONFIGS["small"]
+    rep, _, _ = _full(cfg)
+    assert rep["draft_boundary"] <= 2
+
+
+def test_small_vocab_greedy():
+    _full(W.with_(W.CONFIGS["small"], T=0.0))
+
+
+@pytest.mark.parametrize("name,T,requests", [
+    ("ds", 1.0, [0, 77, 127]),
+    ("ds", 0.0, [5, 126]),
+    ("mixed", 1.0, [0, 127, 128, 255]),
+    ("mixed", 0.0, [1, 200]),
+    ("stress", 1.0, [0, 513, 1023]),
+])
+def test_full_size_sampled(name, T, requests):
+    cfg = W.with_(W.CONFIGS[name], T=T)
+    g = gpu_round(cfg)
+    o = oracle_round(cfg, requests)
+    rep = compare(cfg, g, o, requests)
+    print(json.dumps({k: (float(v) if isinstance(v, float) else v) for k, v in rep.items()}))
+
+
+def test_full_size_invariants_ds():
+    """Properties that hold for every request at full size."""
+    cfg = W.CONFIGS["ds"]
+    g = gpu_round(cfg)
+    R, gamma = cfg.R, cfg.gamma
+    L, A = g["sched_len"], g["accepted_len"]
+    assert np.all((0 <= A) & (A <= L)) and np.all(L <= gamma)
+    assert int(g["K"][0]) == int(L.sum())
+    for r in range(R):
+        assert np.array_equal(g["out_tokens"][r, :A[r]], g["tokens"][r, :A[r]])
+        assert 0 <= g["out_tokens"][r, A[r]] < cfg.V
+        assert np.all(g["out_tokens"][r, A[r] + 1:] == -1)
+    assert np.all((g["q_tok"] > 0) & (g["q_tok"] <= 1))
+    assert np.all((g["tokens"] >= 0) & (g["tokens"] < cfg.V))
+
+
+def test_edge_single_token_vocab_and_block():
+    cfg = W.Workload("v1", R=3, gamma=1, V=1, rank=1, dtype="fp32", T=1.0, mode=W.CAUSAL, seed=3001,
+                     zipf=0.0, target_sd=(0.5,), conf_law="uniform", table="linear", n_table=16)
+    rep, g, _ = _full(cfg)
+    assert np.all(g["tokens"] == 0) and np.all(g["out_tokens"][:, 0] == 0)
+
+
+def test_edge_table_admits_nothing():
+    cfg = W.with_(RAGGED_BF16, n_table=39)  # R = 40 > n_table: nothing scheduled, bonus only
+    rep, g, o = _full(cfg)
+    assert int(g["K"][0]) == 0 and np.all(g["accepted_len"] == 0)
+
+
+def test_worked_round_from_the_pages():
+    here = os.path.dirname(__file__)
+    gld = json.load(open(os.path.join(here, "golden", "worked_round.json")))
+    ids = {c: i for i, c in enumerate(gld["alphabet"])}
+    V, gamma = len(ids), len(gld["draft_rows"])
+    base = np.full((1, gamma, V), gld["off_logit"], np.float32)
+    for k, c in enumerate(gld["draft_rows"]):
+        base[0, k, ids[c]] = 0.0
+    target = np.full((1, gamma + 1, V), gld["off_logit"], np.float32)
+    for k, c in enumerate(gld["target_rows"]):
+        target[0, k, ids[c]] = 0.0
+    dev = "cuda"
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    for T in (1.0, 0.0):
+        for seed in range(4):
+            inp = dict(base=t(base), target=t(target), W1=t(np.zeros((V, 1), np.float32)),
+                       W2=t(np.zeros((1, V), np.float32)), anchor=t(np.array([ids["D"]], np.int32)),
+                       conf=t(np.array([gld["confidences"]], np.float32)), conf_lag=None,
+                       sps=t(np.array(gld["sps"], np.float32)), T=T, seed=seed, mode=W.CAUSAL)
+            g = gpu_round(None, inp)
+            inv = {i: c for c, i in ids.items()}
+            assert [inv[int(x)] for x in g["tokens"][0]] == gld["expected"]["draft"]
+            assert int(g["sched_len"][0]) == gld["expected"]["L"]
+            assert int(g["accepted_len"][0]) == gld["expected"]["A"]
+            emitted = [inv[int(x)] for x in g["out_tokens"][0, :gld["expected"]["A"] + 1]]
+            assert emitted == gld["expected"]["emitted"]
+
+
+def test_nonfinite_confidence_sets_status():
+    cfg = RAGGED_BF16
+    inp = device_inputs(cfg)
+    inp["conf"][3, 1] = float("nan")
+    g = gpu_round(cfg, inp)
+    assert g["status"] == dspark.ERR_NONFINITE
+
+
+def test_bad_anchor_sets_status():
+    cfg = RAGGED_BF16
+    inp = device_inputs(cfg)
+    inp["anchor"][0] = cfg.V + 5
+    g = gpu_round(cfg, inp)
+    assert g["status"] == dspark.ERR_RANGE
+
+
+def test_deterministic_bits():
+    cfg = TC_SHAPE
+    inp = device_inputs(cfg)
+    a = gpu_round(cfg, inp)
+    b = gpu_round(cfg, inp)
+    for k in ("tokens", "q_tok", "q_stats", "sched_len", "out_tokens", "accepted_len", "p_tok", "tau_theta"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_device_generator_matches_numpy():
+    cfg = W.CONFIGS["ds"]
+    base, target = W.logits_device(W.with_(cfg, R=3), "cuda")
+    b_np, t_np = W.logits_rows_np(cfg, [0, 2])
+    bb = base.view(torch.int16).cpu().numpy().view(np.uint16)
+    tt = target.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bb[[0, 2]], b_np) and np.array_equal(tt[[0, 2]], t_np)
+
+
+def test_host_argument_errors_are_synchronous():
+    cfg = RAGGED_BF16
+    inp = device_inputs(cfg)
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dspark.BF16, cfg.n_table)
+    out = dspark.RoundOutputs(R, gamma)
+    with pytest.raises(dspark.DSparkError) as e:
+        dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                      None, inp["sps"], W.LAGGED, 1.0, 0, out, ws)  # LAGGED without lagged conf
+    assert e.value.status == dspark.ERR_INVALID_ARG
+    with pytest.raises(dspark.DSparkError) as e:
+        dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                      None, inp["sps"], W.CAUSAL, 1.0, 0, out, ws[:1024])
+    assert e.value.status == dspark.ERR_WORKSPACE

@@ -72,8 +72,8 @@ class Workload:
 # 7-token block, scheduler off, temperature 1, is about 5.0 (DeepSeek-scale),
 # 5.5 (structured half of the mixed workload) and 3.3 (chat half).
 DS_TARGET_SD = 0.429
-STRUCTURED_TARGET_SD = 0.35
-CHAT_TARGET_SD = 0.85
+STRUCTURED_TARGET_SD = 0.341
+CHAT_TARGET_SD = 0.802
 
 CONFIGS = {
     "tiny": Workload("tiny", R=4, gamma=4, V=64, rank=8, dtype="fp32", T=1.0, mode=CAUSAL,
