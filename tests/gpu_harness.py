@@ -89,8 +89,9 @@ def compare(cfg, g, o, requests, check_schedule=True):
                 lse_g = g["q_stats"][r, k, 0] + T * np.log(g["q_stats"][r, k, 1])
                 lse_o = d["m"][k] + T * np.log(d["Z"][k])
                 assert abs(lse_g - lse_o) < PROB_RTOL * T, f"request {r} q_stats[{k}]"
-            else:
-                assert g["q_stats"][r, k, 0] == np.float32(d["m"][k]) and g["q_stats"][r, k, 1] == 1.0
+            else:  # greedy: the recorded max logit is a float (tolerance); the token is exact
+                assert abs(g["q_stats"][r, k, 0] - d["m"][k]) <= 1e-5 * max(1.0, abs(d["m"][k]))
+                assert g["q_stats"][r, k, 1] == 1.0
         L = int(o["sched"]["L"][r])
         if mis is not None and mis < L:
             rep["verify_excluded"] += 1

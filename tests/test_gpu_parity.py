@@ -78,7 +78,10 @@ def test_full_size_sampled(name, T, requests):
     g = gpu_round(cfg)
     o = oracle_round(cfg, requests)
     rep = compare(cfg, g, o, requests)
-    print(json.dumps({k: (float(v) if isinstance(v, float) else v) for k, v in rep.items()}))
+    rep = {k: (float(v) if isinstance(v, (float, np.floating)) else v) for k, v in rep.items()}
+    os.makedirs("gpurun_out", exist_ok=True)
+    with open(os.path.join("gpurun_out", "parity_reports.jsonl"), "a") as f:
+        f.write(json.dumps({"workload": name, "T": T, "requests": requests, **rep}) + "\n")
 
 
 def test_full_size_invariants_ds():
