@@ -123,7 +123,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="ds")
     ap.add_argument("--temperature", type=float, default=None)
-    ap.add_argument("--cpu-requests", type=int, default=12)
+    ap.add_argument("--cpu-requests", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
