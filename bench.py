@@ -167,10 +167,7 @@ def main():
     __graft_entry__.build()
     from speculative_decoding_draft_seq_gb300 import dspark
 
-    tests_dir = os.path.join(ROOT, "tests")
-    sys.path.insert(0, tests_dir)
-    from gpu_harness import device_inputs
-    inp = device_inputs(cfg, dev)
+    inp = W.device_inputs(cfg, dev)
     R, gamma, V = cfg.R, cfg.gamma, cfg.V
     dt_code = dspark.BF16 if cfg.dtype == "bf16" else dspark.FP32
     ws = dspark.new_workspace(R, gamma, V, cfg.rank, dt_code, cfg.n_table, dev)

@@ -21,13 +21,7 @@ BOUNDARY = 1e-6
 PROB_RTOL = 2e-3
 
 
-def device_inputs(cfg, device="cuda"):
-    base, target = W.logits_device(cfg, device)
-    W1, W2 = W.weights_device(cfg, device)
-    h = W.host_inputs(cfg)
-    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
-    return dict(base=base, target=target, W1=W1, W2=W2, anchor=t(h["anchor"]), conf=t(h["conf"]),
-                conf_lag=t(h["conf_lag"]), sps=t(h["sps"]), T=cfg.T, seed=cfg.philox_seed, mode=cfg.mode)
+device_inputs = W.device_inputs
 
 
 def gpu_round(cfg, inp=None, device="cuda"):

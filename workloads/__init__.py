@@ -383,3 +383,15 @@ def weights_device(cfg, device):
     w1 = _finish_t(cfg, _noise_t(cfg, S_W1, idx, cfg.w_sd, table)).reshape(cfg.V, cfg.rank)
     w2 = _finish_t(cfg, _noise_t(cfg, S_W2, idx, cfg.w_sd, table)).reshape(cfg.rank, cfg.V)
     return w1.contiguous(), w2.contiguous()
+
+
+def device_inputs(cfg, device="cuda"):
+    """Every input of one round as device tensors (torch), for the library."""
+    torch = _torch()
+    base, target = logits_device(cfg, device)
+    W1, W2 = weights_device(cfg, device)
+    h = host_inputs(cfg)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return dict(base=base, target=target, W1=W1, W2=W2, anchor=t(h["anchor"]), conf=t(h["conf"]),
+                conf_lag=t(h["conf_lag"]), sps=t(h["sps"]), T=cfg.T, seed=cfg.philox_seed,
+                mode=cfg.mode)
