@@ -65,7 +65,8 @@ typedef enum {
   DSPARK_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
   DSPARK_ERR_CUDA = 4,        /* a CUDA runtime call failed */
   DSPARK_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (device) */
-  DSPARK_ERR_RANGE = 6        /* a token id outside [0, V) was read (device) */
+  DSPARK_ERR_RANGE = 6,       /* a token id outside [0, V) was read (device) */
+  DSPARK_ERR_TOO_LARGE = 7    /* problem exceeds the fixed scratch of dspark_schedule_static */
 } dspark_status;
 
 typedef enum { DSPARK_FP32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
@@ -143,6 +144,34 @@ dspark_status dspark_schedule(int32_t R, int32_t gamma, const float* conf,
                               int32_t n_table, int32_t mode, int32_t* sched_len,
                               int32_t* K, double* tau_theta, void* workspace,
                               size_t workspace_bytes, dspark_stream_t stream);
+
+/*
+ * dspark_schedule without a workspace, for callers that cannot allocate device
+ * memory. The paper has no counterpart to this entry point: it exists for
+ * callers that run inside an engine which owns all device memory (a reserved
+ * pool sized for weights and KV cache, with no allocator reachable from the
+ * decode step), or that must not risk an allocation failing or fragmenting
+ * memory in the middle of serving. It computes exactly what dspark_schedule
+ * computes, bit for bit, with the same arguments except the workspace.
+ *
+ * Scratch: a fixed array inside the library (393,472 bytes on every GPU that
+ * loads the library, kept until the process exits), so R * gamma must not
+ * exceed 16384; larger problems return DSPARK_ERR_TOO_LARGE and launch
+ * nothing. The call allocates nothing and calls no allocating routine.
+ *   device_status [1] uint32 out, device memory, or NULL: receives this call's
+ *                 device-side status (DSPARK_OK or DSPARK_ERR_NONFINITE), the
+ *                 counterpart of dspark_device_status for this entry point.
+ * The first call on each device looks up the scratch's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call on a device shares the one array, which keeps the last
+ * call's contents: calls that may overlap on the GPU (different streams
+ * without ordering between them) race on it and must not be issued.
+ */
+dspark_status dspark_schedule_static(int32_t R, int32_t gamma, const float* conf,
+                                     const float* conf_lagged, const float* sps_table,
+                                     int32_t n_table, int32_t mode, int32_t* sched_len,
+                                     int32_t* K, double* tau_theta, uint32_t* device_status,
+                                     dspark_stream_t stream);
 
 /*
  * Lossless speculative-sampling verification (GeekNews page, "Definição do

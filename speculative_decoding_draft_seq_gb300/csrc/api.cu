@@ -164,6 +164,7 @@ const char* dspark_status_string(dspark_status status) {
     case DSPARK_ERR_CUDA: return "CUDA runtime error";
     case DSPARK_ERR_TIMEOUT: return "bounded device wait ran out";
     case DSPARK_ERR_RANGE: return "token id outside [0, V)";
+    case DSPARK_ERR_TOO_LARGE: return "R * gamma exceeds the 16384 candidates of the fixed scratch";
   }
   return "unknown status";
 }

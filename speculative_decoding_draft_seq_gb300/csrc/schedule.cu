@@ -283,3 +283,77 @@ cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches
 }
 
 }  // namespace dspark
+
+// ---------------------------------------------------------------------------
+// Scheduler entry point that allocates nothing (dspark_schedule_static).
+//
+// Its scratch is the file-scope array below instead of a caller-provided
+// workspace: a status word, the radix-sort ping-pong buffers and the
+// fixed-point prefix sums for at most kStaticMaxCandidates = R * gamma
+// candidates (393,472 bytes, held by every GPU that loads the library until
+// the process exits). Host code cannot use the array's name as a device
+// address, so the first call on each device looks the address up with
+// cudaGetSymbolAddress (with that device current) and caches it.
+namespace dspark {
+
+constexpr int kStaticMaxCandidates = 16384;
+constexpr size_t kStaticStatusOff = 0;
+constexpr size_t kStaticKey0Off = 256;
+constexpr size_t kStaticKey1Off = kStaticKey0Off + (size_t)kStaticMaxCandidates * 4;
+constexpr size_t kStaticIdx0Off = kStaticKey1Off + (size_t)kStaticMaxCandidates * 4;
+constexpr size_t kStaticIdx1Off = kStaticIdx0Off + (size_t)kStaticMaxCandidates * 4;
+constexpr size_t kStaticFxOff = kStaticIdx1Off + (size_t)kStaticMaxCandidates * 4;
+constexpr size_t kStaticScratchBytes = kStaticFxOff + (size_t)kStaticMaxCandidates * 8;
+
+static __device__ __align__(256) unsigned char g_schedule_scratch[kStaticScratchBytes];
+
+constexpr int kStaticMaxDevices = 64;
+static void* g_schedule_scratch_ptr[kStaticMaxDevices] = {};
+static bool g_schedule_static_attr[kStaticMaxDevices] = {};
+
+}  // namespace dspark
+
+extern "C" dspark_status dspark_schedule_static(int32_t R, int32_t gamma, const float* conf,
+                                                const float* conf_lagged, const float* sps_table,
+                                                int32_t n_table, int32_t mode, int32_t* sched_len,
+                                                int32_t* K, double* tau_theta, uint32_t* device_status,
+                                                dspark_stream_t stream) {
+  using namespace dspark;
+  if (R < 1 || gamma < 1 || n_table < 0) return DSPARK_ERR_INVALID_ARG;
+  if (mode != DSPARK_SCHED_CAUSAL && mode != DSPARK_SCHED_LAGGED && mode != DSPARK_SCHED_ALL)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!conf || !sched_len || !K || !tau_theta || (n_table > 0 && !sps_table)) return DSPARK_ERR_INVALID_ARG;
+  if (mode == DSPARK_SCHED_LAGGED && !conf_lagged) return DSPARK_ERR_INVALID_ARG;
+  if ((long long)R * (long long)gamma > kStaticMaxCandidates) return DSPARK_ERR_TOO_LARGE;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return DSPARK_ERR_CUDA;
+  if (g_schedule_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_schedule_scratch) != cudaSuccess || p == nullptr) return DSPARK_ERR_CUDA;
+    g_schedule_scratch_ptr[dev] = p;
+  }
+  const size_t smem = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
+  if (!g_schedule_static_attr[dev]) {
+    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    g_schedule_static_attr[dev] = true;
+  }
+  char* base = static_cast<char*>(g_schedule_scratch_ptr[dev]);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base + kStaticStatusOff);
+  cudaStream_t s = (cudaStream_t)stream;
+  // The status word is the only scratch that must start at zero; every other
+  // byte a call reads it has written first.
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  schedule_kernel<<<1, kSchedThreads, smem, s>>>(
+      R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta,
+      reinterpret_cast<uint32_t*>(base + kStaticKey0Off), reinterpret_cast<uint32_t*>(base + kStaticKey1Off),
+      reinterpret_cast<uint32_t*>(base + kStaticIdx0Off), reinterpret_cast<uint32_t*>(base + kStaticIdx1Off),
+      reinterpret_cast<unsigned long long*>(base + kStaticFxOff), status);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (device_status != nullptr &&
+      cudaMemcpyAsync(device_status, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}

@@ -14,7 +14,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdspark.so")
 
-OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_RANGE = range(7)
+OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_RANGE, ERR_TOO_LARGE = range(8)
 FP32, BF16 = 0, 1
 CAUSAL, LAGGED, ALL = 0, 1, 2
 
@@ -40,6 +40,8 @@ def _load():
     lib.dspark_draft_sequential.argtypes = [i32] * 5 + [vp] * 4 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
     lib.dspark_schedule.restype = i32
     lib.dspark_schedule.argtypes = [i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.dspark_schedule_static.restype = i32
+    lib.dspark_schedule_static.argtypes = [i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]
     lib.dspark_verify.restype = i32
     lib.dspark_verify.argtypes = [i32] * 5 + [vp] * 9 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
     lib.dspark_round.restype = i32
@@ -115,6 +117,16 @@ def schedule(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, ws, stream=N
     _check(lib.dspark_schedule(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(), int(mode),
                                _ptr(sched_len), _ptr(K), _ptr(tau_theta), _ptr(ws), ws.numel(),
                                _stream(stream)), "dspark_schedule")
+
+
+def schedule_static(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, device_status=None,
+                    stream=None):
+    """dspark_schedule_static: the scheduler without a workspace (fixed library
+    scratch, R * gamma <= 16384). Returns the C status code without raising."""
+    R, gamma = conf.shape
+    return int(lib.dspark_schedule_static(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(),
+                                          int(mode), _ptr(sched_len), _ptr(K), _ptr(tau_theta),
+                                          _ptr(device_status), _stream(stream)))
 
 
 def verify(target, base, anchor, W1, W2, tokens, q_tok, q_stats, sched_len, temperature, seed,
