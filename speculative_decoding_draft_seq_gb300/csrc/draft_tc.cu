@@ -31,7 +31,7 @@ namespace dspark {
 constexpr int kTcM = 128;
 constexpr int kTcKC = 64;   // K rows per W2 stage
 constexpr int kTcBStages = 3;
-constexpr int kTcBaseStages = 3;
+constexpr int kTcBaseStages = 2;  // per epilogue half: each half owns its own ring
 constexpr int kTcEpiWarps = 8;
 constexpr int kTcWarps = 3 + kTcEpiWarps;
 constexpr int kTcThreads = 32 * kTcWarps;
@@ -41,7 +41,7 @@ constexpr uint32_t kBBoxBytes = kTcKC * 128;              // 64 K rows x 64 colu
 constexpr uint32_t kBStageBytes = 4 * kBBoxBytes;         // up to 4 boxes (256 columns)
 constexpr uint32_t kBaseBoxBytes = 128 * 128;             // up to 128 rows x 64 columns
 constexpr uint32_t kTcSmemBytes =
-    1024 + kABytes + kTcBStages * kBStageBytes + kTcBaseStages * kBaseBoxBytes + 1024;
+    1024 + kABytes + kTcBStages * kBStageBytes + 2 * kTcBaseStages * kBaseBoxBytes + 1024;
 
 struct TcParams {
   int R, gamma, V, rank, k;
@@ -74,12 +74,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* sA = smem;
   unsigned char* sB = sA + kABytes;
   unsigned char* sBase = sB + kTcBStages * kBStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + kTcBaseStages * kBaseBoxBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + 2 * kTcBaseStages * kBaseBoxBytes);
   uint64_t* bFull = bars;
   uint64_t* bEmpty = bars + kTcBStages;
-  uint64_t* baseFull = bars + 2 * kTcBStages;
-  uint64_t* baseEmpty = baseFull + kTcBaseStages;
-  uint64_t* accFull = baseEmpty + kTcBaseStages;
+  uint64_t* baseFull = bars + 2 * kTcBStages;        // [half][stage]
+  uint64_t* baseEmpty = baseFull + 2 * kTcBaseStages;
+  uint64_t* accFull = baseEmpty + 2 * kTcBaseStages;
   uint64_t* accEmpty = accFull + 2;
   uint64_t* drain = accEmpty + 2;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(drain + 1);
@@ -95,13 +95,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kTcBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
-    for (int i = 0; i < kTcBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
+    for (int i = 0; i < 2 * kTcBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kTcEpiWarps); }
     mbar_init(drain, 1);
     *sAbort = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(sTmem, 512);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(sTmem, 512);
+  }
   if (tid < kTcM) {
     const int r = m0 + tid;
     int prev = 0;
@@ -155,19 +158,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       prefetch_tensormap(&mapBase);
       const uint64_t pol = l2_policy_evict_first();
       const uint32_t bytes = (uint32_t)p.box_rows * 128;
-      int g = 0;
-      for (int t = 0; t < n_tiles && !*sAbort; ++t) {
+      // Chunk j of a tile goes to epilogue half j & 1. Each half has its own
+      // ring, so every ring has one consumer group that waits on every phase
+      // in order (a parity wait cannot tell phase n from phase n + 2).
+      int nh[2] = {0, 0};
+      bool stop = false;
+      for (int t = 0; t < n_tiles && !stop && !*sAbort; ++t) {
         const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
-        for (int j = 0; j < nbox; ++j, ++g) {
-          const int s = g % kTcBaseStages;
-          const uint32_t ph = (g / kTcBaseStages) & 1;
-          if (!mbar_wait(&baseEmpty[s], ph ^ 1, sAbort, p.status)) break;
-          mbar_expect_tx(&baseFull[s], bytes);
-          tma_load_3d(sBase + s * kBaseBoxBytes, &mapBase, (c0 + j) * 64, p.k - 1, m0, &baseFull[s], pol);
+        for (int j = 0; j < nbox; ++j) {
+          const int h = j & 1, n = nh[h], slot = h * kTcBaseStages + n % kTcBaseStages;
+          if (!mbar_wait(&baseEmpty[slot], ((n / kTcBaseStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+          mbar_expect_tx(&baseFull[slot], bytes);
+          tma_load_3d(sBase + slot * kBaseBoxBytes, &mapBase, (c0 + j) * 64, p.k - 1, m0, &baseFull[slot], pol);
+          nh[h] = n + 1;
         }
       }
-      for (int i = 1; i <= kTcBaseStages && g - i >= 0; ++i)
-        mbar_wait_drain(&baseFull[(g - i) % kTcBaseStages], ((g - i) / kTcBaseStages) & 1, p.status);
+      for (int h = 0; h < 2; ++h)
+        for (int i = 1; i <= kTcBaseStages && nh[h] - i >= 0; ++i) {
+          const int n = nh[h] - i;
+          mbar_wait_drain(&baseFull[h * kTcBaseStages + n % kTcBaseStages], (n / kTcBaseStages) & 1, p.status);
+        }
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
@@ -203,17 +213,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3, h = (warp - 3) >> 2;
     const int row = 32 * q + lane, r = m0 + row;
     const float kT = p.kT;
-    int g_base = 0;  // global index of this tile's first base box
+    int nh = 0;  // boxes this half has consumed from its ring
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1);
       const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
-      if (!mbar_wait(&accFull[buf], use & 1, sAbort, p.status)) break;
+      // every lane waits, then the warp agrees (and reconverges) before the
+      // warp-collective tcgen05.ld below
+      const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(&accFull[buf], use & 1, sAbort, p.status));
+      if (!acc_ok) break;
       tc_fence_after();
       bool ok = true;
       for (int j = h; j < nbox; j += 2) {
-        const int g = g_base + j, s = g % kTcBaseStages;
-        if (!mbar_wait(&baseFull[s], (g / kTcBaseStages) & 1, sAbort, p.status)) { ok = false; break; }
+        const int s = h * kTcBaseStages + nh % kTcBaseStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&baseFull[s], (nh / kTcBaseStages) & 1, sAbort, p.status))) {
+          ok = false;
+          break;
+        }
+        ++nh;
         const unsigned char* brow = sBase + s * kBaseBoxBytes + row * 128;
         const int vbase = (c0 + j) * 64;
         float m = -INFINITY, ssum = 0.f;
@@ -221,6 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float acc[32];
+          __syncwarp();  // tcgen05.ld is warp-collective: the warp must be converged
           tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + half * 32), acc);
           float l[32];
 #pragma unroll
@@ -264,13 +282,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accEmpty[buf]);
-      g_base += nbox;
       if (!ok) break;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
