@@ -1,0 +1,674 @@
+// Persistent tensor-core drafting: all gamma sequential steps in one
+// cooperative launch (bf16 inputs).
+//
+// "DSpark: Aceleração da inferência de LLM com speculative decoding [pdf]"
+// (GeekNews), "Etapa sequencial" / "Head de Markov": at step k each request
+// adds bias = W1[prev, :] . W2 to its base logits of position k and samples
+// token k from the tempered softmax over the vocabulary; prev is the token
+// just sampled at k - 1 (the anchor at k = 1), so the steps are sequential.
+//
+// One CTA per SM, each owning a contiguous range of 64-column chunks of the
+// vocabulary. Per step k:
+//   1. the epilogue warps gather A = W1[prev_r, :] (128 requests per M tile)
+//      into 128-byte-swizzled K-major shared memory;
+//   2. tcgen05 MMAs (one issuing thread) multiply A by TMA-loaded W2 tiles
+//      into TMEM; the epilogue warps add the TMA-loaded base logits and write
+//      per-(request, chunk) softmax partials (max, sum of 2^((l-max)log2e/T))
+//      or (max, argmax) for greedy decoding;
+//   3. grid barrier; the epilogue warps of CTA b draw the tokens of requests
+//      r = b, b + #CTAs, ...: float64 combination of the chunk partials,
+//      inverse CDF to a chunk, recompute of that chunk's 64 logits, float64
+//      prefix sum to the token;
+//   4. grid barrier; the tokens are visible to every CTA for step k + 1.
+// The W2 and base-logit producers do not depend on the sampled tokens, so
+// they keep streaming across steps: the first tiles of step k + 1 load while
+// step k is being located. Every wait (mbarrier or grid barrier) is bounded:
+// when one runs out the kernel records DSPARK_ERR_TIMEOUT, winds down, lets
+// issued copies and MMAs land and frees its TMEM.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace dspark {
+
+constexpr int kPM = 128;        // requests per M tile (MMA M)
+constexpr int kPKC = 64;        // K rows per W2 stage
+constexpr int kPBStages = 3;
+constexpr int kPBaseStages = 2; // per epilogue half
+constexpr int kPEpiWarps = 8;
+constexpr int kPWarps = 3 + kPEpiWarps;
+constexpr int kPThreads = 32 * kPWarps;
+constexpr int kPEpiThreads = 32 * kPEpiWarps;
+constexpr uint32_t kPAChunk = 128 * 128;
+constexpr uint32_t kPABytes = 4 * kPAChunk;
+constexpr uint32_t kPBBox = kPKC * 128;
+constexpr uint32_t kPBStage = 4 * kPBBox;
+constexpr uint32_t kPBaseBox = 128 * 128;
+constexpr uint32_t kPSmem = 1024 + kPABytes + kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox + 1024;
+constexpr uint32_t kGridSpinLimit = 1u << 22;
+
+// Scratch of the locate phase, carved from the A-operand region (free
+// between the last MMA of a step and the next gather).
+constexpr uint32_t kLsW1 = 0;         // float[256]
+constexpr uint32_t kLsRed = 1024;     // float[32][64]
+constexpr uint32_t kLsW = 9216;       // float[64]
+constexpr uint32_t kLsF = 9472;       // float[8]
+constexpr uint32_t kLsI = 9504;       // int[8]
+constexpr uint32_t kLsI2 = 9536;      // int[8]
+constexpr uint32_t kLsD = 9568;       // double[8]
+constexpr uint32_t kLsExcl = 9632;    // double
+constexpr uint32_t kLsG = 9640;       // float
+constexpr uint32_t kLsFlag = 9644;    // int
+
+struct PersistParams {
+  int R, gamma, V, rank;
+  int nc;        // 64-column chunks
+  int n_cta;     // grid size (one CTA per SM)
+  int n_mt;      // 128-request M tiles
+  int box_rows;  // rows of one base box
+  float kT;
+  int greedy;
+  uint64_t seed;
+  const __nv_bfloat16* W1;
+  const __nv_bfloat16* W2;
+  const __nv_bfloat16* base;
+  const int32_t* anchor;
+  int32_t* tokens;
+  float* q_tok;
+  float* q_stats;
+  float2* part;
+  unsigned int* gbar;  // grid-barrier counter, zero at launch
+  uint32_t* status;
+};
+
+__device__ __forceinline__ float px2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Weight of logit l relative to a maximum m, with mk = fl(m * kT).
+__device__ __forceinline__ float pweight(float l, float kT, float mk) { return px2(__fmaf_rn(l, kT, -mk)); }
+
+// --- reductions over the 8 epilogue warps (named barrier 1) --------------
+__device__ __forceinline__ void eg_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ float eg_max(float v, float* sh, int ew, int lane) {
+  v = warp_max(v);
+  if (lane == 0) sh[ew] = v;
+  eg_sync();
+  float r = sh[0];
+#pragma unroll
+  for (int i = 1; i < kPEpiWarps; ++i) r = fmaxf(r, sh[i]);
+  eg_sync();
+  return r;
+}
+__device__ __forceinline__ int eg_min_i(int v, int* sh, int ew, int lane) {
+  v = warp_min_i(v);
+  if (lane == 0) sh[ew] = v;
+  eg_sync();
+  int r = sh[0];
+#pragma unroll
+  for (int i = 1; i < kPEpiWarps; ++i) r = min(r, sh[i]);
+  eg_sync();
+  return r;
+}
+__device__ __forceinline__ int eg_max_i(int v, int* sh, int ew, int lane) {
+  v = warp_max_i(v);
+  if (lane == 0) sh[ew] = v;
+  eg_sync();
+  int r = sh[0];
+#pragma unroll
+  for (int i = 1; i < kPEpiWarps; ++i) r = max(r, sh[i]);
+  eg_sync();
+  return r;
+}
+__device__ __forceinline__ void eg_argmax(float& v, int& idx, float* shf, int* shi, int ew, int lane) {
+  warp_argmax(v, idx);
+  if (lane == 0) { shf[ew] = v; shi[ew] = idx; }
+  eg_sync();
+  v = shf[0];
+  idx = shi[0];
+#pragma unroll
+  for (int i = 1; i < kPEpiWarps; ++i)
+    if (shf[i] > v || (shf[i] == v && shi[i] < idx)) { v = shf[i]; idx = shi[i]; }
+  eg_sync();
+}
+// Exclusive scan of one double per epilogue thread (thread order) + total.
+__device__ __forceinline__ double eg_exscan_d(double v, double* sh, double& total, int ew, int lane) {
+  double x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  double ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = 0.0;
+  if (lane == 31) sh[ew] = x;
+  eg_sync();
+  double before = 0.0, tot = 0.0;
+#pragma unroll
+  for (int i = 0; i < kPEpiWarps; ++i) {
+    if (i < ew) before += sh[i];
+    tot += sh[i];
+  }
+  eg_sync();
+  total = tot;
+  return before + ex;
+}
+
+// Grid-wide barrier among the n_cta CTAs of a cooperative launch: one
+// thread per CTA calls it. Bounded: on timeout it records
+// DSPARK_ERR_TIMEOUT, raises the CTA's abort flag and returns false.
+__device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_t* status,
+                             volatile int* abort) {
+  __threadfence();
+  atomicAdd(counter, 1u);
+  for (uint32_t i = 0; i < kGridSpinLimit; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) {
+      __threadfence();
+      return true;
+    }
+    if (*abort) return false;
+    __nanosleep(64);
+  }
+  atomicCAS(status, 0u, (uint32_t)DSPARK_ERR_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+// Draws token k of request r from the chunk partials (epilogue group of 256
+// threads, et = thread index in the group). `ls` is the locate scratch.
+__device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* ls, int et) {
+  const int ew = et >> 5, lane = et & 31;
+  float* sW1f = reinterpret_cast<float*>(ls + kLsW1);
+  float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
+  float* sW = reinterpret_cast<float*>(ls + kLsW);
+  float* shf = reinterpret_cast<float*>(ls + kLsF);
+  int* shi = reinterpret_cast<int*>(ls + kLsI);
+  int* shi2 = reinterpret_cast<int*>(ls + kLsI2);
+  double* shd = reinterpret_cast<double*>(ls + kLsD);
+  double* sExcl = reinterpret_cast<double*>(ls + kLsExcl);
+  float* sG = reinterpret_cast<float*>(ls + kLsG);
+  int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
+
+  const int nc = p.nc;
+  const float2* pr = p.part + (size_t)r * nc;
+  const size_t out = (size_t)r * p.gamma + (k - 1);
+  const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
+  const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
+  constexpr int kCache = 16;
+  float2 cache[kCache];
+#pragma unroll
+  for (int i = 0; i < kCache; ++i)
+    if (i < c1 - c0) cache[i] = __ldcg(pr + c0 + i);
+  auto get = [&](int c) -> float2 { return (c - c0 < kCache) ? cache[c - c0] : __ldcg(pr + c); };
+
+  if (p.greedy) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = c0; c < c1; ++c) {
+      const float2 q = get(c);
+      const int idx = __float_as_int(q.y);
+      if (q.x > bv || (q.x == bv && idx < bi)) { bv = q.x; bi = idx; }
+    }
+    eg_argmax(bv, bi, shf, shi2, ew, lane);
+    if (et == 0) {
+      __stcg(p.tokens + out, min(max(bi, 0), p.V - 1));
+      p.q_tok[out] = 1.f;
+      p.q_stats[2 * out] = bv;
+      p.q_stats[2 * out + 1] = 1.f;
+    }
+    return;
+  }
+
+  int prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
+  prev = min(max(prev, 0), p.V - 1);
+  for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
+
+  float m = -INFINITY;
+  for (int c = c0; c < c1; ++c) m = fmaxf(m, get(c).x);
+  const float M = eg_max(m, shf, ew, lane);
+  const float kT = p.kT, Mk = __fmul_rn(M, kT);
+  double local = 0.0;
+  for (int c = c0; c < c1; ++c) {
+    const float2 q = get(c);
+    local += (double)q.y * (double)pweight(q.x, kT, Mk);
+  }
+  double Z;
+  const double excl = eg_exscan_d(local, shd, Z, ew, lane);
+  const double u = philox_uniform(p.seed, (uint64_t)r, (uint64_t)k, kDraft);
+  const double target = u * Z;
+  int found = 0x7fffffff, last_pos = -1;
+  double run = excl, found_excl = 0.0;
+  float found_g = 0.f;
+  for (int c = c0; c < c1; ++c) {
+    const float2 q = get(c);
+    const float g = pweight(q.x, kT, Mk);
+    const double f = (double)q.y * (double)g;
+    if (f > 0.0) last_pos = c;
+    if (found == 0x7fffffff) {
+      if (run + f > target) { found = c; found_excl = run; found_g = g; }
+      run += f;
+    }
+  }
+  int cstar = eg_min_i(found, shi, ew, lane);
+  if (found == cstar && cstar != 0x7fffffff) { *sExcl = found_excl; *sG = found_g; *sFlag = 0; }
+  if (cstar == 0x7fffffff) {  // rounding left no crossing: last chunk with mass
+    cstar = max(0, eg_max_i(last_pos, shi, ew, lane));
+    if (et == 0) { *sG = pweight(__ldcg(pr + cstar).x, kT, Mk); *sExcl = 0.0; *sFlag = 1; }
+  }
+  eg_sync();
+
+  // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
+  const int colbase = cstar * kChunk;
+  {
+    const int uc = et & 7, rg = et >> 3;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    if (colbase + uc * 8 < p.V) {
+      for (int i = rg; i < p.rank; i += 32) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.W2 + (size_t)i * p.V + colbase + uc * 8));
+        const float w1 = sW1f[i];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = __fmaf_rn(w1, __uint_as_float(ww[e] << 16), acc[2 * e]);
+          acc[2 * e + 1] = __fmaf_rn(w1, __uint_as_float(ww[e] & 0xffff0000u), acc[2 * e + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[rg][uc * 8 + e] = acc[e];
+  }
+  eg_sync();
+  const float mck = __fmul_rn(__ldcg(pr + cstar).x, kT);
+  if (et < kChunk) {
+    const int v = colbase + et;
+    float w = 0.f;
+    if (v < p.V) {
+      float bias = 0.f;
+#pragma unroll 8
+      for (int g = 0; g < 32; ++g) bias = __fadd_rn(bias, red[g][et]);
+      const float b = __bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + v]);
+      w = pweight(__fadd_rn(b, bias), kT, mck);
+    }
+    sW[et] = w;
+  }
+  eg_sync();
+  if (ew == 0) {  // float64 prefix over the 64 weights: two per lane, warp scan
+    const double g = (double)*sG;
+    const double d0 = (double)sW[2 * lane] * g;
+    const double d1 = d0 + (double)sW[2 * lane + 1] * g;
+    double x = d1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    double ex = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) ex = 0.0;
+    const double base_run = *sExcl + ex;
+    int c = -1;
+    if (!*sFlag) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
+    const unsigned hit = __ballot_sync(0xffffffffu, c >= 0);
+    int xc;
+    if (hit) {
+      xc = __shfl_sync(0xffffffffu, c, __ffs(hit) - 1);
+    } else {  // no crossing inside the chunk: last entry with weight
+      const int lastw = sW[2 * lane + 1] > 0.f ? 2 * lane + 1 : (sW[2 * lane] > 0.f ? 2 * lane : -1);
+      xc = max(0, warp_max_i(lastw));
+    }
+    if (lane == 0) {
+      __stcg(p.tokens + out, min(colbase + xc, p.V - 1));
+      p.q_tok[out] = (float)((double)sW[xc] * g / Z);
+      p.q_stats[2 * out] = M;
+      p.q_stats[2 * out + 1] = (float)Z;
+    }
+  }
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    draft_persistent_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
+                            PersistParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = sA + kPABytes;
+  unsigned char* sBase = sB + kPBStages * kPBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + 2 * kPBaseStages * kPBaseBox);
+  uint64_t* bFull = bars;
+  uint64_t* bEmpty = bFull + kPBStages;
+  uint64_t* baseFull = bEmpty + kPBStages;          // [half][stage]
+  uint64_t* baseEmpty = baseFull + 2 * kPBaseStages;
+  uint64_t* accFull = baseEmpty + 2 * kPBaseStages;
+  uint64_t* accEmpty = accFull + 2;
+  uint64_t* aFull = accEmpty + 2;
+  uint64_t* drain = aFull + 1;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
+  volatile int* sDecide = reinterpret_cast<volatile int*>(sTmem + 2);  // epilogue-group verdict
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c_begin = (int)(((long long)blockIdx.x * p.nc) / p.n_cta);
+  const int c_end = (int)(((long long)(blockIdx.x + 1) * p.nc) / p.n_cta);
+  const int n_tiles = (c_end - c_begin + 3) / 4;
+  const int nkc = p.rank / kPKC;
+
+  if (tid == 0) {
+    for (int i = 0; i < kPBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
+    for (int i = 0; i < 2 * kPBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kPEpiWarps); }
+    mbar_init(aFull, kPEpiWarps);
+    mbar_init(drain, 1);
+    *sAbort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(sTmem, 512);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+
+  if (warp == 0) {
+    if (lane == 0) {  // W2 producer: streams across steps, ahead of the tokens
+      prefetch_tensormap(&mapW2);
+      const uint64_t pol = l2_policy_evict_last();
+      int n = 0;
+      bool stop = false;
+      for (int k = 1; k <= p.gamma && !stop; ++k)
+        for (int mt = 0; mt < p.n_mt && !stop; ++mt)
+          for (int t = 0; t < n_tiles && !stop; ++t) {
+            const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
+            for (int kc = 0; kc < nkc; ++kc) {
+              const int stage = n % kPBStages;
+              if (!mbar_wait(&bEmpty[stage], ((n / kPBStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+              mbar_expect_tx(&bFull[stage], nbox * kPBBox);
+              for (int j = 0; j < nbox; ++j)
+                tma_load_2d(sB + stage * kPBStage + j * kPBBox, &mapW2, (c0 + j) * 64, kc * kPKC, &bFull[stage], pol);
+              ++n;
+            }
+          }
+      for (int i = 1; i <= kPBStages && n - i >= 0; ++i)
+        mbar_wait_drain(&bFull[(n - i) % kPBStages], ((n - i) / kPBStages) & 1, p.status);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {  // base-logit producer: chunk j of a tile -> ring of half j & 1
+      prefetch_tensormap(&mapBase);
+      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t bytes = (uint32_t)p.box_rows * 128;
+      int nh[2] = {0, 0};
+      bool stop = false;
+      for (int k = 1; k <= p.gamma && !stop; ++k)
+        for (int mt = 0; mt < p.n_mt && !stop; ++mt)
+          for (int t = 0; t < n_tiles && !stop; ++t) {
+            const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
+            for (int j = 0; j < nbox; ++j) {
+              const int h = j & 1, n = nh[h], slot = h * kPBaseStages + n % kPBaseStages;
+              if (!mbar_wait(&baseEmpty[slot], ((n / kPBaseStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+              mbar_expect_tx(&baseFull[slot], bytes);
+              tma_load_3d(sBase + slot * kPBaseBox, &mapBase, (c0 + j) * 64, k - 1, mt * kPM, &baseFull[slot], pol);
+              nh[h] = n + 1;
+            }
+          }
+      for (int h = 0; h < 2; ++h)
+        for (int i = 1; i <= kPBaseStages && nh[h] - i >= 0; ++i) {
+          const int n = nh[h] - i;
+          mbar_wait_drain(&baseFull[h * kPBaseStages + n % kPBaseStages], (n / kPBaseStages) & 1, p.status);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      int n = 0, T = 0, a_use = 0;
+      bool stop = false;
+      for (int k = 1; k <= p.gamma && !stop; ++k)
+        for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
+          if (!mbar_wait(aFull, a_use & 1, sAbort, p.status)) { stop = true; break; }
+          ++a_use;
+          tc_fence_after();
+          for (int t = 0; t < n_tiles && !stop; ++t, ++T) {
+            const int buf = T & 1;
+            const uint32_t use = (uint32_t)(T >> 1);
+            if (!mbar_wait(&accEmpty[buf], (use & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+            tc_fence_after();
+            const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
+            const uint32_t idesc = idesc_bf16_f32(kPM, (uint32_t)(64 * nbox), 1);
+            const uint32_t d = tmem + (uint32_t)(buf * 256);
+            for (int kc = 0; kc < nkc; ++kc, ++n) {
+              const int stage = n % kPBStages;
+              if (!mbar_wait(&bFull[stage], (n / kPBStages) & 1, sAbort, p.status)) { stop = true; break; }
+              tc_fence_after();
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + kc * kPAChunk + kk * 32), 0, 1024);
+                const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * kPBStage + kk * 2048), kPBBox, 1024);
+                tc_mma_bf16(d, a_desc, b_desc, idesc, (kc | kk) != 0);
+              }
+              tc_commit(&bEmpty[stage]);
+            }
+            if (stop) break;
+            tc_commit(&accFull[buf]);
+          }
+        }
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, p.status);
+    }
+  } else {
+    // epilogue warps 3..10: A gather, softmax partials, grid barriers, locate
+    const int et = tid - 96, ew = et >> 5;
+    const int q = warp & 3, h = (warp - 3) >> 2;
+    const int row = 32 * q + lane;
+    const float kT = p.kT;
+    int T = 0, nh = 0;
+    unsigned int epoch = 0;
+    bool stop = false;
+    for (int k = 1; k <= p.gamma && !stop; ++k) {
+      for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
+        // A = W1[prev] rows of this M tile (the previous MMAs on sA are done:
+        // every tile of the previous tile sequence was received below)
+        for (int u = et; u < kPM * 32; u += kPEpiThreads) {
+          const int m = u >> 5, j = u & 31, kc = j >> 3, uu = j & 7;
+          const int r = mt * kPM + m;
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (r < p.R && 8 * j < p.rank) {
+            int prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
+            if (prev < 0 || prev >= p.V) {
+              set_status(p.status, DSPARK_ERR_RANGE);
+              prev = min(max(prev, 0), p.V - 1);
+            }
+            val = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.rank + 8 * j));
+          }
+          *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aFull);
+
+        for (int t = 0; t < n_tiles; ++t, ++T) {
+          const int buf = T & 1;
+          const uint32_t use = (uint32_t)(T >> 1);
+          const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
+          if (!__all_sync(0xffffffffu, mbar_wait(&accFull[buf], use & 1, sAbort, p.status))) { stop = true; break; }
+          tc_fence_after();
+          for (int j = h; j < nbox; j += 2) {
+            const int s = h * kPBaseStages + nh % kPBaseStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&baseFull[s], (nh / kPBaseStages) & 1, sAbort, p.status))) {
+              stop = true;
+              break;
+            }
+            ++nh;
+            const unsigned char* brow = sBase + s * kPBaseBox + row * 128;
+            const int vbase = (c0 + j) * 64;
+            float m = -INFINITY, ssum = 0.f;
+            int am = 0x7fffffff;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float acc[32];
+              __syncwarp();
+              tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + half * 32), acc);
+              float l[32];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int unit = half * 4 + u;
+                const uint4 x = *reinterpret_cast<const uint4*>(brow + ((unit ^ (row & 7)) << 4));
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  l[8 * u + 2 * e] = __fadd_rn(__uint_as_float(w[e] << 16), acc[8 * u + 2 * e]);
+                  l[8 * u + 2 * e + 1] = __fadd_rn(__uint_as_float(w[e] & 0xffff0000u), acc[8 * u + 2 * e + 1]);
+                }
+              }
+              const int vh = vbase + half * 32;
+              if (vh + 32 > p.V) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (vh + i >= p.V) l[i] = -INFINITY;
+              }
+              if (p.greedy) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (l[i] > m) { m = l[i]; am = vh + i; }
+              } else {
+                float mh = l[0];
+#pragma unroll
+                for (int i = 1; i < 32; ++i) mh = fmaxf(mh, l[i]);
+                const float mn = fmaxf(m, mh);
+                const float mk = __fmul_rn(mn, kT);
+                float sh = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sh += pweight(l[i], kT, mk);
+                ssum = (m == -INFINITY ? 0.f : ssum * pweight(m, kT, mk)) + sh;
+                m = mn;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&baseEmpty[s]);
+            const int r = mt * kPM + row;
+            if (r < p.R)
+              __stcg(p.part + (size_t)r * p.nc + (c0 + j),
+                     p.greedy ? make_float2(m, __int_as_float(am)) : make_float2(m, ssum));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accEmpty[buf]);
+          if (stop) break;
+        }
+      }
+      // The group never leaves the loop on one warp's say-so: every warp
+      // reaches each named barrier, and the verdict written by one thread
+      // between two barriers is read by all.
+      if (stop) *sAbort = 1;
+      eg_sync();
+      if (et == 0) {  // every CTA has written its partials of step k
+        ++epoch;
+        *sDecide = (*sAbort || !grid_barrier(p.gbar, epoch * (unsigned)p.n_cta, p.status, sAbort)) ? 1 : 0;
+      }
+      eg_sync();
+      if (*sDecide) break;
+      for (int r = blockIdx.x; r < p.R; r += p.n_cta) {
+        locate_row(p, r, k, sA, et);
+        eg_sync();
+      }
+      eg_sync();
+      if (et == 0) {  // every CTA has written its tokens of step k
+        ++epoch;
+        *sDecide = (*sAbort || !grid_barrier(p.gbar, epoch * (unsigned)p.n_cta, p.status, sAbort)) ? 1 : 0;
+      }
+      eg_sync();
+      if (*sDecide) break;
+    }
+    *sAbort = (*sAbort) | (stop ? 1 : 0);  // let the other roles wind down
+    (void)ew;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+bool draft_tc_eligible(const DraftArgs& a);
+
+cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken) {
+  taken = false;
+  if (!draft_tc_eligible(a)) return cudaSuccess;
+  int dev = 0, coop = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaSuccess;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!coop || sms <= 0) return cudaSuccess;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem) !=
+        cudaSuccess)
+      return cudaSuccess;
+    attr = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, draft_persistent_kernel, kPThreads, kPSmem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return cudaSuccess;
+  CUtensorMap mapW2, mapBase;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.V, (uint64_t)a.rank};
+    const uint64_t strides[1] = {(uint64_t)a.V * 2};
+    const uint32_t box[2] = {64, (uint32_t)kPKC};
+    if (!make_tmap_bf16(&mapW2, a.W2, 2, dims, strides, box)) return cudaSuccess;
+  }
+  const int box_rows = a.R < kPM ? a.R : kPM;
+  {
+    const uint64_t dims[3] = {(uint64_t)a.V, (uint64_t)a.gamma, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)a.V * 2, (uint64_t)a.gamma * a.V * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
+    if (!make_tmap_bf16(&mapBase, a.base, 3, dims, strides, box)) return cudaSuccess;
+  }
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  PersistParams p;
+  p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
+  p.nc = ceil_div(a.V, kChunk);
+  p.n_cta = p.nc < sms ? p.nc : sms;
+  p.n_mt = ceil_div(a.R, kPM);
+  p.box_rows = box_rows;
+  p.greedy = a.temperature == 0.f;
+  p.kT = p.greedy ? 0.f : (float)(1.4426950408889634 / (double)a.temperature);
+  p.seed = a.seed;
+  p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
+  p.base = static_cast<const __nv_bfloat16*>(a.base);
+  p.anchor = a.anchor;
+  p.tokens = a.tokens;
+  p.q_tok = a.q_tok;
+  p.q_stats = a.q_stats;
+  p.part = ws_at<float2>(a.ws, L.dpart);
+  p.status = ws_at<uint32_t>(a.ws, L.status);
+  p.gbar = reinterpret_cast<unsigned int*>(p.status + 1);
+  taken = true;
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&mapW2, &mapBase, &p};
+  e = cudaLaunchCooperativeKernel((const void*)draft_persistent_kernel, dim3(p.n_cta), dim3(kPThreads), args,
+                                  kPSmem, s);
+  launches += 1;
+  return e;
+}
+
+}  // namespace dspark
