@@ -79,6 +79,19 @@ struct PersistParams {
   float2* part;
   unsigned int* gbar;  // grid-barrier counter, zero at launch
   uint32_t* status;
+  // residual / bonus pass of verification
+  const __nv_bfloat16* target;  // [R, gamma+1, V]
+  const int4* pend;             // (kind, target row A, prev token, A)
+  const float4* rowstat;        // target row stats (M, Z, argmax, -)
+  int32_t* out_tokens;          // [R, gamma+1]
+  float2* rpart;                // [R][nc] (sum max(0, P - Q), sum P)
+};
+
+// Per-request constants of the residual pass: P(v) = 2^((t_v - M_P) log2e/T) / Z_P
+// from the target row stats, Q(v) from the draft stats of the rejected position.
+struct ResidRow {
+  int kind, A;
+  float MPk, invZP, MQk, invZQ;
 };
 
 __device__ __forceinline__ float px2(float x) {
@@ -88,6 +101,16 @@ __device__ __forceinline__ float px2(float x) {
 }
 // Weight of logit l relative to a maximum m, with mk = fl(m * kT).
 __device__ __forceinline__ float pweight(float l, float kT, float mk) { return px2(__fmaf_rn(l, kT, -mk)); }
+
+// Residual weight max(0, P - Q) (or P for a bonus draw) of one entry; the
+// epilogue and the locate step form it with the same operations. P is
+// returned through `P`.
+__device__ __forceinline__ float resid_w(int kind, float t, float l, const ResidRow& rr, float kT, float& P) {
+  P = __fmul_rn(pweight(t, kT, rr.MPk), rr.invZP);
+  if (kind != kPendResid) return P;
+  const float Q = __fmul_rn(pweight(l, kT, rr.MQk), rr.invZQ);
+  return fmaxf(0.f, __fsub_rn(P, Q));
+}
 
 // --- reductions over the 8 epilogue warps (named barrier 1) --------------
 __device__ __forceinline__ void eg_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -202,20 +225,31 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   const size_t out = (size_t)r * p.gamma + (k - 1);
   const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
   const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
+  // this thread's partials, kept in registers (statically indexed) when the
+  // segment is short enough, else re-read from L2
   constexpr int kCache = 16;
+  const bool cached = c1 - c0 <= kCache;
   float2 cache[kCache];
 #pragma unroll
   for (int i = 0; i < kCache; ++i)
-    if (i < c1 - c0) cache[i] = __ldcg(pr + c0 + i);
-  auto get = [&](int c) -> float2 { return (c - c0 < kCache) ? cache[c - c0] : __ldcg(pr + c); };
+    cache[i] = (cached && i < c1 - c0) ? __ldcg(pr + c0 + i) : make_float2(-INFINITY, 0.f);
 
   if (p.greedy) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = c0; c < c1; ++c) {
-      const float2 q = get(c);
-      const int idx = __float_as_int(q.y);
-      if (q.x > bv || (q.x == bv && idx < bi)) { bv = q.x; bi = idx; }
+    if (cached) {
+#pragma unroll
+      for (int i = 0; i < kCache; ++i) {
+        const float2 q = cache[i];
+        const int idx = __float_as_int(q.y);
+        if (i < c1 - c0 && (q.x > bv || (q.x == bv && idx < bi))) { bv = q.x; bi = idx; }
+      }
+    } else {
+      for (int c = c0; c < c1; ++c) {
+        const float2 q = __ldcg(pr + c);
+        const int idx = __float_as_int(q.y);
+        if (q.x > bv || (q.x == bv && idx < bi)) { bv = q.x; bi = idx; }
+      }
     }
     eg_argmax(bv, bi, shf, shi2, ew, lane);
     if (et == 0) {
@@ -232,13 +266,24 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
 
   float m = -INFINITY;
-  for (int c = c0; c < c1; ++c) m = fmaxf(m, get(c).x);
+  if (cached) {
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) m = fmaxf(m, cache[i].x);
+  } else {
+    for (int c = c0; c < c1; ++c) m = fmaxf(m, __ldcg(pr + c).x);
+  }
   const float M = eg_max(m, shf, ew, lane);
   const float kT = p.kT, Mk = __fmul_rn(M, kT);
   double local = 0.0;
-  for (int c = c0; c < c1; ++c) {
-    const float2 q = get(c);
-    local += (double)q.y * (double)pweight(q.x, kT, Mk);
+  if (cached) {
+#pragma unroll
+    for (int i = 0; i < kCache; ++i)
+      if (i < c1 - c0) local += (double)cache[i].y * (double)pweight(cache[i].x, kT, Mk);
+  } else {
+    for (int c = c0; c < c1; ++c) {
+      const float2 q = __ldcg(pr + c);
+      local += (double)q.y * (double)pweight(q.x, kT, Mk);
+    }
   }
   double Z;
   const double excl = eg_exscan_d(local, shd, Z, ew, lane);
@@ -247,8 +292,7 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   int found = 0x7fffffff, last_pos = -1;
   double run = excl, found_excl = 0.0;
   float found_g = 0.f;
-  for (int c = c0; c < c1; ++c) {
-    const float2 q = get(c);
+  auto visit = [&](int c, float2 q) {
     const float g = pweight(q.x, kT, Mk);
     const double f = (double)q.y * (double)g;
     if (f > 0.0) last_pos = c;
@@ -256,6 +300,13 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       if (run + f > target) { found = c; found_excl = run; found_g = g; }
       run += f;
     }
+  };
+  if (cached) {
+#pragma unroll
+    for (int i = 0; i < kCache; ++i)
+      if (i < c1 - c0) visit(c0 + i, cache[i]);
+  } else {
+    for (int c = c0; c < c1; ++c) visit(c, __ldcg(pr + c));
   }
   int cstar = eg_min_i(found, shi, ew, lane);
   if (found == cstar && cstar != 0x7fffffff) { *sExcl = found_excl; *sG = found_g; *sFlag = 0; }
@@ -267,16 +318,28 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
 
   // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   const int colbase = cstar * kChunk;
+  // base logit of this thread's column, issued together with the W2 loads
+  float bcol = 0.f;
+  if (et < kChunk && colbase + et < p.V)
+    bcol = __bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + colbase + et]);
   {
     const int uc = et & 7, rg = et >> 3;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     if (colbase + uc * 8 < p.V) {
-      for (int i = rg; i < p.rank; i += 32) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.W2 + (size_t)i * p.V + colbase + uc * 8));
-        const float w1 = sW1f[i];
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      uint4 w[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {  // rank <= 256: at most 8 rows per thread
+        const int i = rg + 32 * it;
+        w[it] = i < p.rank ? __ldg(reinterpret_cast<const uint4*>(p.W2 + (size_t)i * p.V + colbase + uc * 8))
+                           : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int i = rg + 32 * it;
+        const float w1 = i < p.rank ? sW1f[i] : 0.f;
+        const uint32_t ww[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           acc[2 * e] = __fmaf_rn(w1, __uint_as_float(ww[e] << 16), acc[2 * e]);
@@ -296,8 +359,7 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       float bias = 0.f;
 #pragma unroll 8
       for (int g = 0; g < 32; ++g) bias = __fadd_rn(bias, red[g][et]);
-      const float b = __bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + v]);
-      w = pweight(__fadd_rn(b, bias), kT, mck);
+      w = pweight(__fadd_rn(bcol, bias), kT, mck);
     }
     sW[et] = w;
   }
@@ -338,8 +400,217 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
 
 namespace dspark {
 
+__device__ __forceinline__ ResidRow load_resid_row(const PersistParams& p, int r) {
+  ResidRow rr;
+  rr.kind = kPendNone;
+  rr.A = 0;
+  rr.MPk = rr.invZP = rr.MQk = rr.invZQ = 0.f;
+  if (r < p.R) {
+    const int4 pd = __ldg(p.pend + r);
+    if (pd.x == kPendResid || pd.x == kPendBonus) {
+      rr.kind = pd.x;
+      rr.A = min(max(pd.y, 0), p.gamma);
+      const float4 rs = __ldg(p.rowstat + (size_t)r * (p.gamma + 1) + rr.A);
+      rr.MPk = __fmul_rn(rs.x, p.kT);
+      rr.invZP = __frcp_rn(rs.y);
+      if (rr.kind == kPendResid) {
+        const size_t qi = 2 * ((size_t)r * p.gamma + min(rr.A, p.gamma - 1));
+        rr.MQk = __fmul_rn(__ldg(p.q_stats + qi), p.kT);
+        rr.invZQ = __frcp_rn(__ldg(p.q_stats + qi + 1));
+      }
+    }
+  }
+  return rr;
+}
+
+__device__ __forceinline__ float unpack_bf16(const uint4& x, int e) {
+  const uint32_t w = e < 2 ? x.x : (e < 4 ? x.y : (e < 6 ? x.z : x.w));
+  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Epilogue of the residual pass for one 64-column chunk of one request: the
+// bias comes from TMEM (two warp-collective loads), the target and base rows
+// of the request's own position A from global memory.
+__device__ __forceinline__ void resid_chunk(const PersistParams& p, const ResidRow& rr, int r, int vbase,
+                                            uint32_t taddr, float& sw, float& sp) {
+  const bool act = rr.kind != kPendNone;
+  uint4 tb[8], bb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { tb[i] = make_uint4(0, 0, 0, 0); bb[i] = make_uint4(0, 0, 0, 0); }
+  if (act) {
+    const uint4* tp = reinterpret_cast<const uint4*>(p.target + ((size_t)r * (p.gamma + 1) + rr.A) * p.V + vbase);
+    const uint4* bp = reinterpret_cast<const uint4*>(p.base + ((size_t)r * p.gamma + min(rr.A, p.gamma - 1)) * p.V + vbase);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (vbase + 8 * i < p.V) {
+        tb[i] = __ldg(tp + i);
+        if (rr.kind == kPendResid) bb[i] = __ldg(bp + i);
+      }
+    }
+  }
+  sw = 0.f;
+  sp = 0.f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float acc[32];
+    __syncwarp();
+    tmem_ld32(taddr + (uint32_t)(half * 32), acc);
+    if (act) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = half * 32 + i;
+        if (vbase + col < p.V) {
+          const float t = unpack_bf16(tb[col >> 3], col & 7);
+          const float l = __fadd_rn(unpack_bf16(bb[col >> 3], col & 7), acc[i]);
+          float P;
+          sw += resid_w(rr.kind, t, l, rr, p.kT, P);
+          sp += P;
+        }
+      }
+    }
+  }
+}
+
+// Draws the corrected (first rejection) or bonus token of request r from the
+// residual chunk sums: inverse CDF over the chunks, recompute of the crossing
+// chunk, float64 prefix within it. Falls back to P when the residual has no
+// mass.
+__device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* ls, int et) {
+  const int ew = et >> 5, lane = et & 31;
+  float* sW1f = reinterpret_cast<float*>(ls + kLsW1);
+  float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
+  float* sW = reinterpret_cast<float*>(ls + kLsW);
+  int* shi = reinterpret_cast<int*>(ls + kLsI);
+  double* shd = reinterpret_cast<double*>(ls + kLsD);
+  double* sExcl = reinterpret_cast<double*>(ls + kLsExcl);
+  int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
+
+  const ResidRow rr = load_resid_row(p, r);
+  if (rr.kind == kPendNone) return;  // same for every thread of the group
+  const int4 pd = __ldg(p.pend + r);
+  const int prev = min(max(pd.z, 0), p.V - 1);
+  if (rr.kind == kPendResid)
+    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
+
+  const int nc = p.nc;
+  const float2* pr = p.rpart + (size_t)r * nc;
+  const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
+  const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
+  double lres = 0.0, lp = 0.0;
+  for (int c = c0; c < c1; ++c) {
+    const float2 q = __ldcg(pr + c);
+    lres += (double)q.x;
+    lp += (double)q.y;
+  }
+  double W;
+  double excl = eg_exscan_d(lres, shd, W, ew, lane);
+  const bool use_p = !(W > 0.0);  // group-uniform
+  if (use_p) excl = eg_exscan_d(lp, shd, W, ew, lane);
+  const int kind = use_p ? kPendBonus : rr.kind;
+  const uint64_t purpose = rr.kind == kPendResid ? kResid : kBonus;
+  const double u = philox_uniform(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose);
+  const double target = u * W;
+  int found = 0x7fffffff, last_pos = -1;
+  double run = excl, found_excl = 0.0;
+  for (int c = c0; c < c1; ++c) {
+    const float2 q = __ldcg(pr + c);
+    const double f = (double)(use_p ? q.y : q.x);
+    if (f > 0.0) last_pos = c;
+    if (found == 0x7fffffff) {
+      if (run + f > target) { found = c; found_excl = run; }
+      run += f;
+    }
+  }
+  int cstar = eg_min_i(found, shi, ew, lane);
+  if (found == cstar && cstar != 0x7fffffff) { *sExcl = found_excl; *sFlag = 0; }
+  if (cstar == 0x7fffffff) {
+    cstar = max(0, eg_max_i(last_pos, shi, ew, lane));
+    if (et == 0) { *sExcl = 0.0; *sFlag = 1; }
+  }
+  eg_sync();
+
+  const int colbase = cstar * kChunk;
+  float tcol = 0.f, bcol = 0.f;
+  if (et < kChunk && colbase + et < p.V) {
+    tcol = __bfloat162float(p.target[((size_t)r * (p.gamma + 1) + rr.A) * p.V + colbase + et]);
+    if (kind == kPendResid)
+      bcol = __bfloat162float(p.base[((size_t)r * p.gamma + min(rr.A, p.gamma - 1)) * p.V + colbase + et]);
+  }
+  if (kind == kPendResid) {  // bias of the 64 columns (group-uniform branch)
+    const int uc = et & 7, rg = et >> 3;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    if (colbase + uc * 8 < p.V) {
+      uint4 w[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int i = rg + 32 * it;
+        w[it] = i < p.rank ? __ldg(reinterpret_cast<const uint4*>(p.W2 + (size_t)i * p.V + colbase + uc * 8))
+                           : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int i = rg + 32 * it;
+        const float w1 = i < p.rank ? sW1f[i] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(w1, unpack_bf16(w[it], e), acc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[rg][uc * 8 + e] = acc[e];
+  }
+  eg_sync();
+  if (et < kChunk) {
+    float w = 0.f;
+    if (colbase + et < p.V) {
+      float bias = 0.f;
+      if (kind == kPendResid) {
+#pragma unroll 8
+        for (int g = 0; g < 32; ++g) bias = __fadd_rn(bias, red[g][et]);
+      }
+      float P;
+      w = resid_w(kind, tcol, __fadd_rn(bcol, bias), rr, p.kT, P);
+    }
+    sW[et] = w;
+  }
+  eg_sync();
+  if (ew == 0) {
+    const double d0 = (double)sW[2 * lane];
+    const double d1 = d0 + (double)sW[2 * lane + 1];
+    double x = d1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    double ex = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) ex = 0.0;
+    const double base_run = *sExcl + ex;
+    int c = -1;
+    if (!*sFlag) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
+    const unsigned hit = __ballot_sync(0xffffffffu, c >= 0);
+    int xc;
+    if (hit) {
+      xc = __shfl_sync(0xffffffffu, c, __ffs(hit) - 1);
+    } else {
+      const int lastw = sW[2 * lane + 1] > 0.f ? 2 * lane + 1 : (sW[2 * lane] > 0.f ? 2 * lane : -1);
+      xc = max(0, warp_max_i(lastw));
+    }
+    if (lane == 0) p.out_tokens[(size_t)r * (p.gamma + 1) + rr.A] = min(colbase + xc, p.V - 1);
+  }
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+// kResid = false: the gamma drafting steps. kResid = true: one pass of the
+// verifier's residual / bonus draw (A rows = W1[prev] of each request's
+// first rejected position, per-request target and base rows read directly).
+template <bool kResid>
 __global__ void __launch_bounds__(kPThreads, 1)
-    draft_persistent_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
+    persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                             PersistParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -364,6 +635,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int c_end = (int)(((long long)(blockIdx.x + 1) * p.nc) / p.n_cta);
   const int n_tiles = (c_end - c_begin + 3) / 4;
   const int nkc = p.rank / kPKC;
+  const int n_steps = kResid ? 1 : p.gamma;
 
   if (tid == 0) {
     for (int i = 0; i < kPBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
@@ -389,7 +661,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint64_t pol = l2_policy_evict_last();
       int n = 0;
       bool stop = false;
-      for (int k = 1; k <= p.gamma && !stop; ++k)
+      for (int k = 1; k <= n_steps && !stop; ++k)
         for (int mt = 0; mt < p.n_mt && !stop; ++mt)
           for (int t = 0; t < n_tiles && !stop; ++t) {
             const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
@@ -406,13 +678,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_wait_drain(&bFull[(n - i) % kPBStages], ((n - i) / kPBStages) & 1, p.status);
     }
   } else if (warp == 2) {
-    if (lane == 0) {  // base-logit producer: chunk j of a tile -> ring of half j & 1
+    if (!kResid && lane == 0) {  // base-logit producer: chunk j of a tile -> ring of half j & 1
       prefetch_tensormap(&mapBase);
       const uint64_t pol = l2_policy_evict_first();
       const uint32_t bytes = (uint32_t)p.box_rows * 128;
       int nh[2] = {0, 0};
       bool stop = false;
-      for (int k = 1; k <= p.gamma && !stop; ++k)
+      for (int k = 1; k <= n_steps && !stop; ++k)
         for (int mt = 0; mt < p.n_mt && !stop; ++mt)
           for (int t = 0; t < n_tiles && !stop; ++t) {
             const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
@@ -434,7 +706,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {  // MMA issuer
       int n = 0, T = 0, a_use = 0;
       bool stop = false;
-      for (int k = 1; k <= p.gamma && !stop; ++k)
+      for (int k = 1; k <= n_steps && !stop; ++k)
         for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
           if (!mbar_wait(aFull, a_use & 1, sAbort, p.status)) { stop = true; break; }
           ++a_use;
@@ -474,28 +746,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
     int T = 0, nh = 0;
     unsigned int epoch = 0;
     bool stop = false;
-    for (int k = 1; k <= p.gamma && !stop; ++k) {
+    for (int k = 1; k <= n_steps && !stop; ++k) {
       for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
         // A = W1[prev] rows of this M tile (the previous MMAs on sA are done:
         // every tile of the previous tile sequence was received below)
-        for (int u = et; u < kPM * 32; u += kPEpiThreads) {
-          const int m = u >> 5, j = u & 31, kc = j >> 3, uu = j & 7;
-          const int r = mt * kPM + m;
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (r < p.R && 8 * j < p.rank) {
-            int prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
+        {  // two threads per row: one token load, then 16 independent 16-byte loads
+          const int m = et >> 1, j0 = (et & 1) * 16, r = mt * kPM + m;
+          int prev = -1;
+          if (kResid) {
+            if (r < p.R) {
+              const int4 pd = __ldg(p.pend + r);
+              prev = (pd.x == kPendResid) ? min(max(pd.z, 0), p.V - 1) : -1;
+            }
+          } else if (r < p.R) {
+            prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
             if (prev < 0 || prev >= p.V) {
               set_status(p.status, DSPARK_ERR_RANGE);
               prev = min(max(prev, 0), p.V - 1);
             }
-            val = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.rank + 8 * j));
           }
-          *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val;
+          const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)max(prev, 0) * p.rank);
+          uint4 val[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            val[i] = (prev >= 0 && 8 * (j0 + i) < p.rank) ? __ldg(src + j0 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = j0 + i, kc = j >> 3, uu = j & 7;
+            *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val[i];
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(aFull);
 
+        ResidRow rr{};
+        if (kResid) rr = load_resid_row(p, mt * kPM + row);
         for (int t = 0; t < n_tiles; ++t, ++T) {
           const int buf = T & 1;
           const uint32_t use = (uint32_t)(T >> 1);
@@ -503,6 +789,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (!__all_sync(0xffffffffu, mbar_wait(&accFull[buf], use & 1, sAbort, p.status))) { stop = true; break; }
           tc_fence_after();
           for (int j = h; j < nbox; j += 2) {
+            if (kResid) {
+              const int r = mt * kPM + row;
+              float sw, sp;
+              resid_chunk(p, rr, r, (c0 + j) * 64,
+                          tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), sw, sp);
+              if (rr.kind != kPendNone) __stcg(p.rpart + (size_t)r * p.nc + (c0 + j), make_float2(sw, sp));
+              continue;
+            }
             const int s = h * kPBaseStages + nh % kPBaseStages;
             if (!__all_sync(0xffffffffu, mbar_wait(&baseFull[s], (nh / kPBaseStages) & 1, sAbort, p.status))) {
               stop = true;
@@ -578,16 +872,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
       eg_sync();
       if (*sDecide) break;
       for (int r = blockIdx.x; r < p.R; r += p.n_cta) {
-        locate_row(p, r, k, sA, et);
+        if (kResid)
+          locate_resid_row(p, r, sA, et);
+        else
+          locate_row(p, r, k, sA, et);
         eg_sync();
       }
-      eg_sync();
-      if (et == 0) {  // every CTA has written its tokens of step k
-        ++epoch;
-        *sDecide = (*sAbort || !grid_barrier(p.gbar, epoch * (unsigned)p.n_cta, p.status, sAbort)) ? 1 : 0;
+      if (!kResid) {
+        eg_sync();
+        if (et == 0) {  // every CTA has written its tokens of step k
+          ++epoch;
+          *sDecide = (*sAbort || !grid_barrier(p.gbar, epoch * (unsigned)p.n_cta, p.status, sAbort)) ? 1 : 0;
+        }
+        eg_sync();
+        if (*sDecide) break;
       }
-      eg_sync();
-      if (*sDecide) break;
     }
     *sAbort = (*sAbort) | (stop ? 1 : 0);  // let the other roles wind down
     (void)ew;
@@ -617,13 +916,13 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   if (!coop || sms <= 0) return cudaSuccess;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(draft_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(persistent_sweep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPSmem) != cudaSuccess)
       return cudaSuccess;
     attr = true;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, draft_persistent_kernel, kPThreads, kPSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<false>, kPThreads, kPSmem) !=
           cudaSuccess ||
       per_sm < 1)
     return cudaSuccess;
@@ -665,7 +964,76 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   void* args[] = {&mapW2, &mapBase, &p};
-  e = cudaLaunchCooperativeKernel((const void*)draft_persistent_kernel, dim3(p.n_cta), dim3(kPThreads), args,
+  e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<false>, dim3(p.n_cta), dim3(kPThreads), args,
+                                  kPSmem, s);
+  launches += 1;
+  return e;
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+// The verifier's residual / bonus draw on the tensor cores: one cooperative
+// launch of the sweep kernel in residual mode. Returns taken = false (and
+// launches nothing) when the shape or the device does not allow it.
+cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& launches, bool& taken) {
+  taken = false;
+  if (a.temperature == 0.f) return cudaSuccess;
+  DraftArgs d{a.R, a.gamma, a.V, a.rank, a.dtype, a.base, a.anchor, a.W1, a.W2, a.temperature, a.seed,
+              nullptr, nullptr, nullptr, a.ws};
+  if (!draft_tc_eligible(d) || (reinterpret_cast<uintptr_t>(a.target) & 15) != 0) return cudaSuccess;
+  int dev = 0, coop = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaSuccess;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!coop || sms <= 0) return cudaSuccess;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(persistent_sweep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPSmem) != cudaSuccess)
+      return cudaSuccess;
+    attr = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<true>, kPThreads, kPSmem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return cudaSuccess;
+  CUtensorMap mapW2;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.V, (uint64_t)a.rank};
+    const uint64_t strides[1] = {(uint64_t)a.V * 2};
+    const uint32_t box[2] = {64, (uint32_t)kPKC};
+    if (!make_tmap_bf16(&mapW2, a.W2, 2, dims, strides, box)) return cudaSuccess;
+  }
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  PersistParams p{};
+  p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
+  p.nc = ceil_div(a.V, kChunk);
+  p.n_cta = p.nc < sms ? p.nc : sms;
+  p.n_mt = ceil_div(a.R, kPM);
+  p.box_rows = a.R < kPM ? a.R : kPM;
+  p.greedy = 0;
+  p.kT = (float)(1.4426950408889634 / (double)a.temperature);
+  p.seed = a.seed;
+  p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
+  p.base = static_cast<const __nv_bfloat16*>(a.base);
+  p.anchor = a.anchor;
+  p.q_stats = const_cast<float*>(a.q_stats);
+  p.status = ws_at<uint32_t>(a.ws, L.status);
+  p.gbar = reinterpret_cast<unsigned int*>(p.status + 1);
+  p.target = static_cast<const __nv_bfloat16*>(a.target);
+  p.pend = ws_at<int4>(a.ws, L.pend);
+  p.rowstat = ws_at<float4>(a.ws, L.rowstat);
+  p.out_tokens = a.out_tokens;
+  p.rpart = ws_at<float2>(a.ws, L.rpart);
+  taken = true;
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&mapW2, &mapW2, &p};  // no base map in residual mode
+  e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
   return e;

@@ -22,6 +22,8 @@
 
 namespace dspark {
 
+cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& launches, bool& taken);
+
 constexpr int kStatThreads = 512;
 constexpr int kRRows = 32;
 constexpr int kRKBlock = 32;
@@ -344,6 +346,9 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
                                                           a.out_tokens, a.accepted_len, pend);
   launches += 2;
   if (!greedy) {
+    bool taken = false;
+    cudaError_t e = launch_resid_persistent(a, s, launches, taken);
+    if (taken || e != cudaSuccess) return e == cudaSuccess ? cudaGetLastError() : e;
     const int nc = ceil_div(a.V, kChunk);
     resid_partials_kernel<Tin><<<dim3(nc, ceil_div(a.R, kRRows)), 256, 0, s>>>(
         a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats, rowstat, pend, kT, rpart);
