@@ -76,7 +76,9 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uin
 // increments; u = (2 * (w0 >> 12) + 1) * 2^-53 is an exact double in (0, 1).
 enum Purpose : uint64_t { kDraft = 0, kAccept = 1, kResid = 2, kBonus = 3 };
 
-__device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t r, uint64_t k, uint64_t purpose) {
+// The odd integer 2 * (w0 >> 12) + 1 < 2^53 of U(seed, r, k, purpose):
+// u = philox_odd53(...) * 2^-53 exactly.
+__device__ __forceinline__ uint64_t philox_odd53(uint64_t seed, uint64_t r, uint64_t k, uint64_t purpose) {
   const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
   const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
   uint64_t c0 = r, c1 = k, c2 = purpose, c3 = 0;
@@ -89,7 +91,30 @@ __device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t r, uint
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
     k0 += W0; k1 += W1;
   }
-  return (double)(2ull * (c0 >> 12) + 1ull) * 0x1p-53;
+  return 2ull * (c0 >> 12) + 1ull;
+}
+
+// floor(u * Z) for u = odd53 * 2^-53 and an integer Z < 2^64 (exact, 128-bit product).
+__device__ __forceinline__ unsigned long long scale_u53(uint64_t odd53, unsigned long long Z) {
+  const unsigned long long hi = __umul64hi(odd53, Z), lo = odd53 * Z;
+  return (hi << 11) | (lo >> 53);
+}
+
+// floor(f * 2^40) for a finite float f >= 0, exactly, with integer operations
+// (values below 2^-40 give 0). Masses up to 2^23 fit without overflow.
+__device__ __forceinline__ unsigned long long fx40(float f) {
+  const uint32_t b = __float_as_uint(f);
+  const int e = (int)((b >> 23) & 0xFFu);
+  if (e == 0 || (b >> 31)) return 0ull;
+  const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 127 - 23 + 40;
+  if (sh >= 0) return m << sh;
+  if (sh <= -24) return 0ull;
+  return m >> (-sh);
+}
+
+__device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t r, uint64_t k, uint64_t purpose) {
+  return (double)philox_odd53(seed, r, k, purpose) * 0x1p-53;
 }
 
 // ---------------------------------------------------------------------------

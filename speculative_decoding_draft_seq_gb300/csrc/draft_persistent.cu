@@ -55,8 +55,8 @@ constexpr uint32_t kLsW = 9216;       // float[64]
 constexpr uint32_t kLsF = 9472;       // float[8]
 constexpr uint32_t kLsI = 9504;       // int[8]
 constexpr uint32_t kLsI2 = 9536;      // int[8]
-constexpr uint32_t kLsD = 9568;       // double[8]
-constexpr uint32_t kLsExcl = 9632;    // double
+constexpr uint32_t kLsD = 9568;       // u64[8]
+constexpr uint32_t kLsExcl = 9632;    // u64
 constexpr uint32_t kLsG = 9640;       // float
 constexpr uint32_t kLsFlag = 9644;    // int
 
@@ -156,19 +156,23 @@ __device__ __forceinline__ void eg_argmax(float& v, int& idx, float* shf, int* s
     if (shf[i] > v || (shf[i] == v && shi[i] < idx)) { v = shf[i]; idx = shi[i]; }
   eg_sync();
 }
-// Exclusive scan of one double per epilogue thread (thread order) + total.
-__device__ __forceinline__ double eg_exscan_d(double v, double* sh, double& total, int ew, int lane) {
-  double x = v;
+// Exclusive scan of one unsigned 64-bit integer per epilogue thread (thread
+// order) + total and this thread's inclusive value; integer adds are exact,
+// so the intervals [exclusive, inclusive) tile [0, total).
+__device__ __forceinline__ unsigned long long eg_exscan_u64(unsigned long long v, unsigned long long* sh,
+                                                            unsigned long long& total, int ew, int lane,
+                                                            unsigned long long& inclusive) {
+  unsigned long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  double ex = __shfl_up_sync(0xffffffffu, x, 1);
-  if (lane == 0) ex = 0.0;
+  unsigned long long ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = 0ull;
   if (lane == 31) sh[ew] = x;
   eg_sync();
-  double before = 0.0, tot = 0.0;
+  unsigned long long before = 0ull, tot = 0ull;
 #pragma unroll
   for (int i = 0; i < kPEpiWarps; ++i) {
     if (i < ew) before += sh[i];
@@ -176,7 +180,18 @@ __device__ __forceinline__ double eg_exscan_d(double v, double* sh, double& tota
   }
   eg_sync();
   total = tot;
+  inclusive = before + x;
   return before + ex;
+}
+
+// Inclusive warp scan of unsigned 64-bit integers.
+__device__ __forceinline__ unsigned long long warp_inscan_u64(unsigned long long x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
 }
 
 // Grid-wide barrier among the n_cta CTAs of a cooperative launch: one
@@ -194,7 +209,7 @@ __device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_
       return true;
     }
     if (*abort) return false;
-    __nanosleep(64);
+    if (i > 64) __nanosleep(32);
   }
   atomicCAS(status, 0u, (uint32_t)DSPARK_ERR_TIMEOUT);
   *abort = 1;
@@ -215,8 +230,8 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   float* shf = reinterpret_cast<float*>(ls + kLsF);
   int* shi = reinterpret_cast<int*>(ls + kLsI);
   int* shi2 = reinterpret_cast<int*>(ls + kLsI2);
-  double* shd = reinterpret_cast<double*>(ls + kLsD);
-  double* sExcl = reinterpret_cast<double*>(ls + kLsExcl);
+  unsigned long long* shd = reinterpret_cast<unsigned long long*>(ls + kLsD);
+  unsigned long long* sExcl = reinterpret_cast<unsigned long long*>(ls + kLsExcl);
   float* sG = reinterpret_cast<float*>(ls + kLsG);
   int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
 
@@ -264,6 +279,8 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   int prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
   prev = min(max(prev, 0), p.V - 1);
   for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
+  unsigned long long* shu = shd;
+  unsigned long long* sExclU = sExcl;
 
   float m = -INFINITY;
   if (cached) {
@@ -274,51 +291,79 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   }
   const float M = eg_max(m, shf, ew, lane);
   const float kT = p.kT, Mk = __fmul_rn(M, kT);
-  double local = 0.0;
+  // chunk masses f_c = s_c * 2^((m_c - M) log2e/T) (one float32 rounding),
+  // summed exactly as 2^-40 fixed-point integers
+  unsigned long long local = 0ull;
+  int last_pos = -1;
   if (cached) {
 #pragma unroll
     for (int i = 0; i < kCache; ++i)
-      if (i < c1 - c0) local += (double)cache[i].y * (double)pweight(cache[i].x, kT, Mk);
+      if (i < c1 - c0) {
+        const unsigned long long f = fx40(__fmul_rn(cache[i].y, pweight(cache[i].x, kT, Mk)));
+        if (f) last_pos = c0 + i;
+        local += f;
+      }
   } else {
     for (int c = c0; c < c1; ++c) {
       const float2 q = __ldcg(pr + c);
-      local += (double)q.y * (double)pweight(q.x, kT, Mk);
+      const unsigned long long f = fx40(__fmul_rn(q.y, pweight(q.x, kT, Mk)));
+      if (f) last_pos = c;
+      local += f;
     }
   }
-  double Z;
-  const double excl = eg_exscan_d(local, shd, Z, ew, lane);
-  const double u = philox_uniform(p.seed, (uint64_t)r, (uint64_t)k, kDraft);
-  const double target = u * Z;
-  int found = 0x7fffffff, last_pos = -1;
-  double run = excl, found_excl = 0.0;
-  float found_g = 0.f;
-  auto visit = [&](int c, float2 q) {
-    const float g = pweight(q.x, kT, Mk);
-    const double f = (double)q.y * (double)g;
-    if (f > 0.0) last_pos = c;
-    if (found == 0x7fffffff) {
-      if (run + f > target) { found = c; found_excl = run; found_g = g; }
+  if (et == 0) *sFlag = 1;  // "no owner" until the owner clears it
+  unsigned long long Z, incl;
+  const unsigned long long excl = eg_exscan_u64(local, shu, Z, ew, lane, incl);
+  const unsigned long long target = scale_u53(philox_odd53(p.seed, (uint64_t)r, (uint64_t)k, kDraft), Z);
+  if (excl <= target && target < incl) {  // the one thread whose segment holds the crossing
+    unsigned long long run = excl, found_excl = excl;
+    int found = -1;
+    float found_g = 0.f, found_m = 0.f;
+    auto visit = [&](int c, float2 q) {
+      const float g = pweight(q.x, kT, Mk);
+      const unsigned long long f = fx40(__fmul_rn(q.y, g));
+      if (found < 0 && run + f > target) { found = c; found_excl = run; found_g = g; found_m = q.x; }
       run += f;
-    }
-  };
-  if (cached) {
+    };
+    if (cached) {
 #pragma unroll
-    for (int i = 0; i < kCache; ++i)
-      if (i < c1 - c0) visit(c0 + i, cache[i]);
-  } else {
-    for (int c = c0; c < c1; ++c) visit(c, __ldcg(pr + c));
+      for (int i = 0; i < kCache; ++i)
+        if (i < c1 - c0) visit(c0 + i, cache[i]);
+    } else {
+      for (int c = c0; c < c1 && found < 0; ++c) visit(c, __ldcg(pr + c));
+    }
+    if (found < 0) {
+      found = max(c0, last_pos);
+      const float2 q = __ldcg(pr + found);
+      found_g = pweight(q.x, kT, Mk);
+      found_m = q.x;
+    }
+    *sExclU = found_excl;
+    *sG = found_g;
+    shf[0] = found_m;
+    shi2[0] = found;
+    *sFlag = 0;
   }
-  int cstar = eg_min_i(found, shi, ew, lane);
-  if (found == cstar && cstar != 0x7fffffff) { *sExcl = found_excl; *sG = found_g; *sFlag = 0; }
-  if (cstar == 0x7fffffff) {  // rounding left no crossing: last chunk with mass
+  eg_sync();
+  int cstar;
+  const int fallback = *sFlag;
+  if (fallback) {  // no owner (cannot happen for Z > 0): last chunk with mass
     cstar = max(0, eg_max_i(last_pos, shi, ew, lane));
-    if (et == 0) { *sG = pweight(__ldcg(pr + cstar).x, kT, Mk); *sExcl = 0.0; *sFlag = 1; }
+    if (et == 0) {
+      const float2 q = __ldcg(pr + cstar);
+      *sG = pweight(q.x, kT, Mk);
+      *sExclU = 0ull;
+      shf[0] = q.x;
+    }
+    eg_sync();
+  } else {
+    cstar = shi2[0];
   }
+  const float mck = __fmul_rn(shf[0], kT);
   eg_sync();
 
   // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   const int colbase = cstar * kChunk;
-  // base logit of this thread's column, issued together with the W2 loads
   float bcol = 0.f;
   if (et < kChunk && colbase + et < p.V)
     bcol = __bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + colbase + et]);
@@ -351,7 +396,6 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     for (int e = 0; e < 8; ++e) red[rg][uc * 8 + e] = acc[e];
   }
   eg_sync();
-  const float mck = __fmul_rn(__ldcg(pr + cstar).x, kT);
   if (et < kChunk) {
     const int v = colbase + et;
     float w = 0.f;
@@ -364,21 +408,16 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     sW[et] = w;
   }
   eg_sync();
-  if (ew == 0) {  // float64 prefix over the 64 weights: two per lane, warp scan
-    const double g = (double)*sG;
-    const double d0 = (double)sW[2 * lane] * g;
-    const double d1 = d0 + (double)sW[2 * lane + 1] * g;
-    double x = d1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    double ex = __shfl_up_sync(0xffffffffu, x, 1);
-    if (lane == 0) ex = 0.0;
-    const double base_run = *sExcl + ex;
+  if (ew == 0) {  // fixed-point prefix over the 64 weights: two per lane, warp scan
+    const float g = *sG;
+    const unsigned long long d0 = fx40(__fmul_rn(sW[2 * lane], g));
+    const unsigned long long d1 = d0 + fx40(__fmul_rn(sW[2 * lane + 1], g));
+    const unsigned long long x = warp_inscan_u64(d1, lane);
+    unsigned long long ex = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) ex = 0ull;
+    const unsigned long long base_run = *sExclU + ex;
     int c = -1;
-    if (!*sFlag) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
+    if (!fallback) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
     const unsigned hit = __ballot_sync(0xffffffffu, c >= 0);
     int xc;
     if (hit) {
@@ -387,11 +426,15 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       const int lastw = sW[2 * lane + 1] > 0.f ? 2 * lane + 1 : (sW[2 * lane] > 0.f ? 2 * lane : -1);
       xc = max(0, warp_max_i(lastw));
     }
+    const int tok = min(colbase + xc, p.V - 1);
+    if (lane < 4 && k < p.gamma)  // the next step gathers W1[tok]: bring its 512 bytes into L2 now
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.W1 + (size_t)tok * p.rank + lane * 64));
     if (lane == 0) {
-      __stcg(p.tokens + out, min(colbase + xc, p.V - 1));
-      p.q_tok[out] = (float)((double)sW[xc] * g / Z);
+      const float Zf = __fmul_rn((float)Z, 0x1p-40f);
+      __stcg(p.tokens + out, tok);
+      p.q_tok[out] = __fdiv_rn(__fmul_rn(sW[xc], g), Zf);
       p.q_stats[2 * out] = M;
-      p.q_stats[2 * out + 1] = (float)Z;
+      p.q_stats[2 * out + 1] = Zf;
     }
   }
 }
@@ -481,8 +524,8 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
   float* sW = reinterpret_cast<float*>(ls + kLsW);
   int* shi = reinterpret_cast<int*>(ls + kLsI);
-  double* shd = reinterpret_cast<double*>(ls + kLsD);
-  double* sExcl = reinterpret_cast<double*>(ls + kLsExcl);
+  unsigned long long* shd = reinterpret_cast<unsigned long long*>(ls + kLsD);
+  unsigned long long* sExcl = reinterpret_cast<unsigned long long*>(ls + kLsExcl);
   int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
 
   const ResidRow rr = load_resid_row(p, r);
@@ -494,38 +537,79 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
 
   const int nc = p.nc;
   const float2* pr = p.rpart + (size_t)r * nc;
+  unsigned long long* shu = shd;
+  unsigned long long* sExclU = sExcl;
   const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
   const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
-  double lres = 0.0, lp = 0.0;
-  for (int c = c0; c < c1; ++c) {
-    const float2 q = __ldcg(pr + c);
-    lres += (double)q.x;
-    lp += (double)q.y;
-  }
-  double W;
-  double excl = eg_exscan_d(lres, shd, W, ew, lane);
-  const bool use_p = !(W > 0.0);  // group-uniform
-  if (use_p) excl = eg_exscan_d(lp, shd, W, ew, lane);
-  const int kind = use_p ? kPendBonus : rr.kind;
-  const uint64_t purpose = rr.kind == kPendResid ? kResid : kBonus;
-  const double u = philox_uniform(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose);
-  const double target = u * W;
-  int found = 0x7fffffff, last_pos = -1;
-  double run = excl, found_excl = 0.0;
-  for (int c = c0; c < c1; ++c) {
-    const float2 q = __ldcg(pr + c);
-    const double f = (double)(use_p ? q.y : q.x);
-    if (f > 0.0) last_pos = c;
-    if (found == 0x7fffffff) {
-      if (run + f > target) { found = c; found_excl = run; }
-      run += f;
+  constexpr int kCache = 16;  // this thread's chunk sums, statically indexed
+  const bool cached = c1 - c0 <= kCache;
+  float2 cache[kCache];
+#pragma unroll
+  for (int i = 0; i < kCache; ++i)
+    cache[i] = (cached && i < c1 - c0) ? __ldcg(pr + c0 + i) : make_float2(0.f, 0.f);
+  auto getp = [&](int i) -> float2 { return cached ? cache[i] : __ldcg(pr + c0 + i); };
+  unsigned long long lres = 0ull, lp = 0ull;
+  if (cached) {
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) { lres += fx40(cache[i].x); lp += fx40(cache[i].y); }
+  } else {
+    for (int c = c0; c < c1; ++c) {
+      const float2 q = __ldcg(pr + c);
+      lres += fx40(q.x);
+      lp += fx40(q.y);
     }
   }
-  int cstar = eg_min_i(found, shi, ew, lane);
-  if (found == cstar && cstar != 0x7fffffff) { *sExcl = found_excl; *sFlag = 0; }
-  if (cstar == 0x7fffffff) {
+  unsigned long long W, incl;
+  unsigned long long excl = eg_exscan_u64(lres, shu, W, ew, lane, incl);
+  const bool use_p = W == 0ull;  // group-uniform: empty residual under rounding
+  if (use_p) excl = eg_exscan_u64(lp, shu, W, ew, lane, incl);
+  const int kind = use_p ? kPendBonus : rr.kind;
+  const uint64_t purpose = rr.kind == kPendResid ? kResid : kBonus;
+  const unsigned long long target = scale_u53(philox_odd53(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose), W);
+  if (et == 0) *sFlag = 1;
+  eg_sync();
+  int last_pos = -1;
+  if (cached) {
+#pragma unroll
+    for (int i = 0; i < kCache; ++i)
+      if (i < c1 - c0 && fx40(use_p ? cache[i].y : cache[i].x)) last_pos = c0 + i;
+  } else {
+    for (int c = c0; c < c1; ++c)
+      if (fx40(use_p ? __ldcg(pr + c).y : __ldcg(pr + c).x)) last_pos = c;
+  }
+  if (excl <= target && target < incl) {  // the one owner of the crossing
+    unsigned long long run = excl, found_excl = excl;
+    int found = -1;
+    if (cached) {
+#pragma unroll
+      for (int i = 0; i < kCache; ++i)
+        if (i < c1 - c0) {
+          const unsigned long long f = fx40(use_p ? cache[i].y : cache[i].x);
+          if (found < 0 && run + f > target) { found = c0 + i; found_excl = run; }
+          run += f;
+        }
+    } else {
+      for (int c = c0; c < c1 && found < 0; ++c) {
+        const float2 q = getp(c - c0);
+        const unsigned long long f = fx40(use_p ? q.y : q.x);
+        if (run + f > target) { found = c; found_excl = run; }
+        run += f;
+      }
+    }
+    if (found < 0) found = max(c0, last_pos);
+    *sExclU = found_excl;
+    shi[0] = found;
+    *sFlag = 0;
+  }
+  eg_sync();
+  const int fallback = *sFlag;
+  int cstar;
+  if (fallback) {
     cstar = max(0, eg_max_i(last_pos, shi, ew, lane));
-    if (et == 0) { *sExcl = 0.0; *sFlag = 1; }
+    if (et == 0) *sExclU = 0ull;
+    eg_sync();
+  } else {
+    cstar = shi[0];
   }
   eg_sync();
 
@@ -576,19 +660,14 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   }
   eg_sync();
   if (ew == 0) {
-    const double d0 = (double)sW[2 * lane];
-    const double d1 = d0 + (double)sW[2 * lane + 1];
-    double x = d1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    double ex = __shfl_up_sync(0xffffffffu, x, 1);
-    if (lane == 0) ex = 0.0;
-    const double base_run = *sExcl + ex;
+    const unsigned long long d0 = fx40(sW[2 * lane]);
+    const unsigned long long d1 = d0 + fx40(sW[2 * lane + 1]);
+    const unsigned long long x = warp_inscan_u64(d1, lane);
+    unsigned long long ex = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) ex = 0ull;
+    const unsigned long long base_run = *sExclU + ex;
     int c = -1;
-    if (!*sFlag) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
+    if (!fallback) c = (base_run + d0 > target) ? 2 * lane : ((base_run + d1 > target) ? 2 * lane + 1 : -1);
     const unsigned hit = __ballot_sync(0xffffffffu, c >= 0);
     int xc;
     if (hit) {
@@ -807,11 +886,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int vbase = (c0 + j) * 64;
             float m = -INFINITY, ssum = 0.f;
             int am = 0x7fffffff;
+            uint32_t accr[64];
+            __syncwarp();
+            tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), accr);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               float acc[32];
-              __syncwarp();
-              tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + half * 32), acc);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(accr[half * 32 + i]);
               float l[32];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {

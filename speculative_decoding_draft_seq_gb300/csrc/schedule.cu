@@ -20,6 +20,10 @@ namespace dspark {
 
 constexpr int kSchedThreads = 1024;
 constexpr int kDigits = 16;
+// Up to this many candidates the sort keys and indices live in shared memory.
+constexpr int kSmemKeys = 8192;
+constexpr size_t kCntBytes = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
+constexpr size_t kSchedSmemMax = kCntBytes + 4 * (size_t)kSmemKeys * sizeof(uint32_t);
 
 // Exclusive scan of one unsigned 64-bit value per thread; returns the total.
 __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v,
@@ -57,8 +61,18 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
 __device__ __forceinline__ uint32_t survival_key(float a) { return 0x3F800000u - __float_as_uint(a); }
 __device__ __forceinline__ float key_survival(uint32_t key) { return __uint_as_float(0x3F800000u - key); }
 
+// floor(a * 2^40 + 1/2) for a float32 a in [0, 1], with integer operations
+// (equal to the same expression evaluated exactly in float64).
 __device__ __forceinline__ unsigned long long fixed_point(float a) {
-  return __double2ull_rz(__dadd_rn(__dmul_rn((double)a, 1099511627776.0), 0.5));
+  const uint32_t b = __float_as_uint(a);
+  const int e = (int)((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;  // zero or subnormal: below 2^-41
+  const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 110;  // a * 2^40 = m * 2^(e - 110)
+  if (sh >= 0) return m << sh;
+  const int s = -sh;
+  if (s > 40) return 0ull;
+  return (m + (1ull << (s - 1))) >> s;
 }
 
 __device__ __forceinline__ double theta_of(int R, unsigned long long S, float sps) {
@@ -67,12 +81,16 @@ __device__ __forceinline__ double theta_of(int R, unsigned long long S, float sp
 }
 
 // Survival keys of one confidence matrix; flags non-finite entries.
+// `stage` (n words) receives the confidences in one coalesced pass first.
 __device__ void build_keys(const float* conf, int R, int gamma, uint32_t* key, uint32_t* idx,
-                           uint32_t* status) {
+                           uint32_t* stage, uint32_t* status) {
+  const int n = R * gamma;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) stage[i] = __float_as_uint(__ldg(conf + i));
+  __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     float acc = 1.f;
     for (int j = 0; j < gamma; ++j) {
-      float c = conf[(size_t)r * gamma + j];
+      float c = __uint_as_float(stage[(size_t)r * gamma + j]);
       if (!isfinite(c)) {
         set_status(status, DSPARK_ERR_NONFINITE);
         c = 0.f;
@@ -148,13 +166,20 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ sps, int n_table, int mode, int32_t* __restrict__ L,
     int32_t* __restrict__ Kout, double* __restrict__ tau_theta, uint32_t* key0, uint32_t* key1,
     uint32_t* idx0, uint32_t* idx1, unsigned long long* fx, uint32_t* status) {
-  extern __shared__ uint32_t cnt[];  // kDigits * blockDim.x
+  extern __shared__ uint32_t cnt[];  // kDigits * blockDim.x, then the keys when they fit
   __shared__ unsigned long long shu[32];
   __shared__ int shi[32];
   __shared__ double shd[32];
   __shared__ int sBad;
   const int tid = threadIdx.x, T = blockDim.x;
   const int n = R * gamma;
+  if (n <= kSmemKeys) {  // sort in shared memory
+    uint32_t* sk = cnt + kDigits * kSchedThreads;
+    key0 = sk;
+    key1 = sk + kSmemKeys;
+    idx0 = sk + 2 * kSmemKeys;
+    idx1 = sk + 3 * kSmemKeys;
+  }
 
   if (tid == 0) sBad = 0;
   __syncthreads();
@@ -174,7 +199,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
 
   if (mode == DSPARK_SCHED_ALL) {
-    build_keys(conf, R, gamma, key0, idx0, status);
+    build_keys(conf, R, gamma, key0, idx0, key1, status);
     unsigned long long loc = 0;
     for (int i = tid; i < n; i += T) loc += fixed_point(key_survival(key0[i]));
     unsigned long long tot;
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 
   int K = 0;
   if (mode == DSPARK_SCHED_LAGGED) {
-    build_keys(conf_lag, R, gamma, key0, idx0, status);
+    build_keys(conf_lag, R, gamma, key0, idx0, key1, status);
     radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
     fixed_prefix(key0, n, fx, shu);
     const int imax = min(n, n_table - R);
@@ -233,7 +258,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     __syncthreads();
   }
 
-  build_keys(conf, R, gamma, key0, idx0, status);
+  build_keys(conf, R, gamma, key0, idx0, key1, status);
   radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
   fixed_prefix(key0, n, fx, shu);
 
@@ -267,10 +292,11 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches) {
   const WsLayout L = ws_layout(a.R, a.gamma, 1);
   void* ws = a.ws;
-  const size_t smem = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
+  const size_t smem = kCntBytes + ((long long)a.R * a.gamma <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSchedSmemMax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -333,9 +359,9 @@ extern "C" dspark_status dspark_schedule_static(int32_t R, int32_t gamma, const 
     if (cudaGetSymbolAddress(&p, g_schedule_scratch) != cudaSuccess || p == nullptr) return DSPARK_ERR_CUDA;
     g_schedule_scratch_ptr[dev] = p;
   }
-  const size_t smem = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
+  const size_t smem = kCntBytes + ((long long)R * gamma <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
   if (!g_schedule_static_attr[dev]) {
-    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSchedSmemMax) !=
         cudaSuccess)
       return DSPARK_ERR_CUDA;
     g_schedule_static_attr[dev] = true;

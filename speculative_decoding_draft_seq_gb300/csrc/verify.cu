@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
     float* __restrict__ p_tok, uint32_t* status) {
   __shared__ float shf[32];
   __shared__ int shi[32];
-  __shared__ double shd[32];
+  __shared__ unsigned long long shu[32];
   const int r = blockIdx.x, k = blockIdx.y, tid = threadIdx.x;
   const int L = min(max(sched_len[r], 0), gamma);
   if (k > L) return;
@@ -86,16 +86,23 @@ __global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
   OnlineStat st;
   // per-thread spans are interleaved in 8-element groups (coalesced 16-byte loads)
   if (sizeof(Tin) == 2 && (V & 7) == 0) {
+    // four 16-byte loads in flight per thread per iteration (HBM latency)
     const uint4* p = reinterpret_cast<const uint4*>(target + row);
-    const int ng = V >> 3;
-    for (int g = tid; g < ng; g += blockDim.x) {
-      const uint4 q = __ldg(p + g);
-      float t[8];
-      t[0] = bf16_bits_to_float(q.x & 0xffffu); t[1] = bf16_bits_to_float(q.x >> 16);
-      t[2] = bf16_bits_to_float(q.y & 0xffffu); t[3] = bf16_bits_to_float(q.y >> 16);
-      t[4] = bf16_bits_to_float(q.z & 0xffffu); t[5] = bf16_bits_to_float(q.z >> 16);
-      t[6] = bf16_bits_to_float(q.w & 0xffffu); t[7] = bf16_bits_to_float(q.w >> 16);
-      st.add8(t, g * 8, kT, greedy);
+    const int ng = V >> 3, T = blockDim.x;
+    for (int g0 = tid; g0 < ng; g0 += 4 * T) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = (g0 + u * T < ng) ? __ldg(p + g0 + u * T) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (g0 + u * T >= ng) continue;
+        float t[8];
+        t[0] = bf16_bits_to_float(q[u].x & 0xffffu); t[1] = bf16_bits_to_float(q[u].x >> 16);
+        t[2] = bf16_bits_to_float(q[u].y & 0xffffu); t[3] = bf16_bits_to_float(q[u].y >> 16);
+        t[4] = bf16_bits_to_float(q[u].z & 0xffffu); t[5] = bf16_bits_to_float(q[u].z >> 16);
+        t[6] = bf16_bits_to_float(q[u].w & 0xffffu); t[7] = bf16_bits_to_float(q[u].w >> 16);
+        st.add8(t, (g0 + u * T) * 8, kT, greedy);
+      }
     }
   } else {
     for (int v = tid; v < V; v += blockDim.x) st.add1(ld_elem(target, row + v), v, kT, greedy);
@@ -103,21 +110,30 @@ __global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
   float am = st.am;
   int ai = st.ai;
   block_argmax(am, ai, shf, shi);
-  float M = 0.f;
-  double Z = 1.0;
+  float M = 0.f, Zf = 1.f;
   if (!greedy) {
+    // Z = sum over threads of s_t * 2^((m_t - M) log2e/T), each term rounded
+    // once in float32 and summed exactly as 2^-40 fixed-point integers
     M = block_max(st.m, shf);
-    const double contrib = st.s > 0.f ? (double)st.s * (double)target_weight(st.m, M, kT) : 0.0;
-    block_exscan_d(contrib, shd, Z);
+    const float contrib = st.s > 0.f ? __fmul_rn(st.s, target_weight(st.m, M, kT)) : 0.f;
+    unsigned long long v = fx40(contrib);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((tid & 31) == 0) shu[tid >> 5] = v;
+    __syncthreads();
+    unsigned long long Z = 0ull;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) Z += shu[i];
+    Zf = __fmul_rn((float)Z, 0x1p-40f);
   }
   if (tid == 0) {
-    rowstat[(size_t)r * (gamma + 1) + k] = make_float4(M, (float)Z, __int_as_float(ai), 0.f);
+    rowstat[(size_t)r * (gamma + 1) + k] = make_float4(M, Zf, __int_as_float(ai), 0.f);
     if (k < L) {
       int x = tokens[(size_t)r * gamma + k];
       if (x < 0 || x >= V) { set_status(status, DSPARK_ERR_RANGE); x = min(max(x, 0), V - 1); }
       float p;
       if (greedy) p = (x == ai) ? 1.f : 0.f;
-      else p = (float)((double)target_weight(ld_elem(target, row + x), M, kT) / Z);
+      else p = __fdiv_rn(target_weight(ld_elem(target, row + x), M, kT), Zf);
       p_tok[(size_t)r * gamma + k] = p;
     }
   }
