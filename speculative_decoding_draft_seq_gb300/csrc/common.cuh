@@ -28,6 +28,7 @@ struct WsLayout {
   size_t rowstat;  // float4 [R][gamma+1]    target row stats (M, Z, argmax, unused)
   size_t pend;     // int4   [R]             (kind, target row, prev token, accepted)
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
+  size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
   size_t skey0, skey1, sidx0, sidx1;  // u32 [R*gamma] radix-sort ping-pong
   size_t fx;       // u64 [R*gamma]         fixed-point prefix sums in sorted order
   size_t total;
@@ -43,6 +44,7 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.rowstat = o; o = align256(o + (size_t)R * (gamma + 1) * sizeof(float4));
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
   L.rpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
+  L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
   L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));
   L.skey1 = o;   o = align256(o + n * sizeof(uint32_t));
   L.sidx0 = o;   o = align256(o + n * sizeof(uint32_t));

@@ -59,6 +59,8 @@ constexpr uint32_t kLsD = 9568;       // u64[8]
 constexpr uint32_t kLsExcl = 9632;    // u64
 constexpr uint32_t kLsG = 9640;       // float
 constexpr uint32_t kLsFlag = 9644;    // int
+constexpr uint32_t kLsW1Blk = 16384;  // bf16[64][rank]: W1 rows of the crossing chunk
+constexpr int kCache = 8;             // chunk partials per thread kept in registers (V <= 131072)
 
 struct PersistParams {
   int R, gamma, V, rank;
@@ -78,6 +80,7 @@ struct PersistParams {
   float* q_stats;
   float2* part;
   unsigned int* gbar;  // grid-barrier counter, zero at launch
+  __nv_bfloat16* astage;  // [2][R][rank] W1 rows of the drawn tokens, by step parity
   uint32_t* status;
   // residual / bonus pass of verification
   const __nv_bfloat16* target;  // [R, gamma+1, V]
@@ -195,19 +198,17 @@ __device__ __forceinline__ unsigned long long warp_inscan_u64(unsigned long long
 }
 
 // Grid-wide barrier among the n_cta CTAs of a cooperative launch: one
-// thread per CTA calls it. Bounded: on timeout it records
-// DSPARK_ERR_TIMEOUT, raises the CTA's abort flag and returns false.
+// thread per CTA calls it, after a CTA barrier that follows the writes it
+// publishes. The arrival is a release add (no value awaited) and the poll an
+// acquire load. Bounded: on timeout it records DSPARK_ERR_TIMEOUT, raises the
+// CTA's abort flag and returns false.
 __device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_t* status,
                              volatile int* abort) {
-  __threadfence();
-  atomicAdd(counter, 1u);
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
   for (uint32_t i = 0; i < kGridSpinLimit; ++i) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
-    if (v >= target) {
-      __threadfence();
-      return true;
-    }
+    if (v >= target) return true;
     if (*abort) return false;
     if (i > 64) __nanosleep(32);
   }
@@ -221,8 +222,13 @@ __device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_
 namespace dspark {
 
 // Draws token k of request r from the chunk partials (epilogue group of 256
-// threads, et = thread index in the group). `ls` is the locate scratch.
-__device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* ls, int et) {
+// threads, et = thread index in the group). `ls` is the locate scratch. When a
+// step k + 1 follows, the W1 row of the drawn token is staged in
+// astage[k & 1][r], the A-operand row of request r for that step; the 64 W1
+// rows of the crossing chunk are fetched into shared memory (bulk copy counted
+// on w1Full, use number w1_use) while the chunk's logits are recomputed.
+__device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* ls, int et, uint64_t* w1Full,
+                           uint32_t& w1_use) {
   const int ew = et >> 5, lane = et & 31;
   float* sW1f = reinterpret_cast<float*>(ls + kLsW1);
   float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
@@ -230,19 +236,21 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   float* shf = reinterpret_cast<float*>(ls + kLsF);
   int* shi = reinterpret_cast<int*>(ls + kLsI);
   int* shi2 = reinterpret_cast<int*>(ls + kLsI2);
-  unsigned long long* shd = reinterpret_cast<unsigned long long*>(ls + kLsD);
-  unsigned long long* sExcl = reinterpret_cast<unsigned long long*>(ls + kLsExcl);
+  unsigned long long* shu = reinterpret_cast<unsigned long long*>(ls + kLsD);
+  unsigned long long* sExclU = reinterpret_cast<unsigned long long*>(ls + kLsExcl);
   float* sG = reinterpret_cast<float*>(ls + kLsG);
   int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
+  const unsigned char* sBlk = ls + kLsW1Blk;
 
   const int nc = p.nc;
   const float2* pr = p.part + (size_t)r * nc;
   const size_t out = (size_t)r * p.gamma + (k - 1);
+  const bool stage_next = k < p.gamma;
+  uint4* stage = reinterpret_cast<uint4*>(p.astage + ((size_t)(k & 1) * p.R + r) * p.rank);
   const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
   const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
   // this thread's partials, kept in registers (statically indexed) when the
   // segment is short enough, else re-read from L2
-  constexpr int kCache = 16;
   const bool cached = c1 - c0 <= kCache;
   float2 cache[kCache];
 #pragma unroll
@@ -267,20 +275,34 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       }
     }
     eg_argmax(bv, bi, shf, shi2, ew, lane);
+    const int tok = min(max(bi, 0), p.V - 1);
+    if (ew == 0 && stage_next && 8 * lane < p.rank) {  // 16 bytes of the W1 row per lane
+      stage[lane] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)tok * p.rank) + lane);
+      fence_proxy_async_global();
+    }
     if (et == 0) {
-      __stcg(p.tokens + out, min(max(bi, 0), p.V - 1));
+      __stcg(p.tokens + out, tok);
       p.q_tok[out] = 1.f;
       p.q_stats[2 * out] = bv;
       p.q_stats[2 * out + 1] = 1.f;
     }
+    fence_proxy_async_smem();  // the scratch is overwritten next by a TMA load of the A operand
     return;
   }
 
-  int prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
-  prev = min(max(prev, 0), p.V - 1);
-  for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
-  unsigned long long* shu = shd;
-  unsigned long long* sExclU = sExcl;
+  // W1 row of the previous token: the anchor's at k = 1, else the row this
+  // CTA staged when it drew token k - 1 of this request
+  if (k == 1) {
+    const int a = min(max(__ldg(p.anchor + r), 0), p.V - 1);
+    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)a * p.rank + i]);
+  } else {
+    const __nv_bfloat16* prev_row = p.astage + ((size_t)((k - 1) & 1) * p.R + r) * p.rank;
+    for (int i = et; i < p.rank; i += kPEpiThreads) {
+      const unsigned short h = __ldcg(reinterpret_cast<const unsigned short*>(prev_row) + i);
+      sW1f[i] = __uint_as_float((uint32_t)h << 16);
+    }
+  }
+  const uint64_t odd = philox_odd53(p.seed, (uint64_t)r, (uint64_t)k, kDraft);
 
   float m = -INFINITY;
   if (cached) {
@@ -289,7 +311,15 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   } else {
     for (int c = c0; c < c1; ++c) m = fmaxf(m, __ldcg(pr + c).x);
   }
-  const float M = eg_max(m, shf, ew, lane);
+  // group maximum: one barrier (the slots are not written again before the
+  // next row's draw, which is behind later barriers)
+  m = warp_max(m);
+  if (lane == 0) shf[ew] = m;
+  if (et == 0) *sFlag = 1;  // "no owner" until the owner clears it
+  eg_sync();
+  float M = shf[0];
+#pragma unroll
+  for (int i = 1; i < kPEpiWarps; ++i) M = fmaxf(M, shf[i]);
   const float kT = p.kT, Mk = __fmul_rn(M, kT);
   // chunk masses f_c = s_c * 2^((m_c - M) log2e/T) (one float32 rounding),
   // summed exactly as 2^-40 fixed-point integers
@@ -311,26 +341,39 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       local += f;
     }
   }
-  if (et == 0) *sFlag = 1;  // "no owner" until the owner clears it
-  unsigned long long Z, incl;
-  const unsigned long long excl = eg_exscan_u64(local, shu, Z, ew, lane, incl);
-  const unsigned long long target = scale_u53(philox_odd53(p.seed, (uint64_t)r, (uint64_t)k, kDraft), Z);
+  // exclusive scan over the group: one barrier
+  const unsigned long long xin = warp_inscan_u64(local, lane);
+  if (lane == 31) shu[ew] = xin;
+  eg_sync();
+  unsigned long long before = 0ull, Z = 0ull;
+#pragma unroll
+  for (int i = 0; i < kPEpiWarps; ++i) {
+    if (i < ew) before += shu[i];
+    Z += shu[i];
+  }
+  const unsigned long long incl = before + xin, excl = incl - local;
+  const unsigned long long target = scale_u53(odd, Z);
   if (excl <= target && target < incl) {  // the one thread whose segment holds the crossing
     unsigned long long run = excl, found_excl = excl;
     int found = -1;
     float found_g = 0.f, found_m = 0.f;
-    auto visit = [&](int c, float2 q) {
-      const float g = pweight(q.x, kT, Mk);
-      const unsigned long long f = fx40(__fmul_rn(q.y, g));
-      if (found < 0 && run + f > target) { found = c; found_excl = run; found_g = g; found_m = q.x; }
-      run += f;
-    };
     if (cached) {
 #pragma unroll
       for (int i = 0; i < kCache; ++i)
-        if (i < c1 - c0) visit(c0 + i, cache[i]);
+        if (i < c1 - c0) {
+          const float g = pweight(cache[i].x, kT, Mk);
+          const unsigned long long f = fx40(__fmul_rn(cache[i].y, g));
+          if (found < 0 && run + f > target) { found = c0 + i; found_excl = run; found_g = g; found_m = cache[i].x; }
+          run += f;
+        }
     } else {
-      for (int c = c0; c < c1 && found < 0; ++c) visit(c, __ldcg(pr + c));
+      for (int c = c0; c < c1 && found < 0; ++c) {
+        const float2 q = __ldcg(pr + c);
+        const float g = pweight(q.x, kT, Mk);
+        const unsigned long long f = fx40(__fmul_rn(q.y, g));
+        if (run + f > target) { found = c; found_excl = run; found_g = g; found_m = q.x; }
+        run += f;
+      }
     }
     if (found < 0) {
       found = max(c0, last_pos);
@@ -360,10 +403,14 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     cstar = shi2[0];
   }
   const float mck = __fmul_rn(shf[0], kT);
-  eg_sync();
 
-  // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   const int colbase = cstar * kChunk;
+  if (stage_next && et == 0) {  // the candidate W1 rows, while the chunk is recomputed
+    const uint32_t bytes = (uint32_t)(min(kChunk, p.V - colbase) * p.rank * 2);
+    mbar_expect_tx(w1Full, bytes);
+    bulk_load(ls + kLsW1Blk, p.W1 + (size_t)colbase * p.rank, bytes, w1Full);
+  }
+  // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   float bcol = 0.f;
   if (et < kChunk && colbase + et < p.V)
     bcol = __bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + colbase + et]);
@@ -427,8 +474,13 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       xc = max(0, warp_max_i(lastw));
     }
     const int tok = min(colbase + xc, p.V - 1);
-    if (lane < 4 && k < p.gamma)  // the next step gathers W1[tok]: bring its 512 bytes into L2 now
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.W1 + (size_t)tok * p.rank + lane * 64));
+    if (stage_next) {  // copy W1[tok] from the fetched chunk rows to the staging row
+      mbar_wait_drain(w1Full, w1_use & 1, p.status);
+      if (8 * lane < p.rank) {
+        stage[lane] = *reinterpret_cast<const uint4*>(sBlk + (size_t)(tok - colbase) * p.rank * 2 + 16 * lane);
+        fence_proxy_async_global();
+      }
+    }
     if (lane == 0) {
       const float Zf = __fmul_rn((float)Z, 0x1p-40f);
       __stcg(p.tokens + out, tok);
@@ -437,6 +489,8 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       p.q_stats[2 * out + 1] = Zf;
     }
   }
+  if (stage_next) ++w1_use;
+  fence_proxy_async_smem();  // the scratch is overwritten next by a TMA load of the A operand
 }
 
 }  // namespace dspark
@@ -541,7 +595,6 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   unsigned long long* sExclU = sExcl;
   const int seg = (nc + kPEpiThreads - 1) / kPEpiThreads;
   const int c0 = min(nc, et * seg), c1 = min(nc, c0 + seg);
-  constexpr int kCache = 16;  // this thread's chunk sums, statically indexed
   const bool cached = c1 - c0 <= kCache;
   float2 cache[kCache];
 #pragma unroll
@@ -690,7 +743,7 @@ namespace dspark {
 template <bool kResid>
 __global__ void __launch_bounds__(kPThreads, 1)
     persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
-                            PersistParams p) {
+                            const __grid_constant__ CUtensorMap mapA, PersistParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sA = smem;
@@ -705,7 +758,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* accEmpty = accFull + 2;
   uint64_t* aFull = accEmpty + 2;
   uint64_t* drain = aFull + 1;
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* w1Full = drain + 1;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(w1Full + 1);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   volatile int* sDecide = reinterpret_cast<volatile int*>(sTmem + 2);  // epilogue-group verdict
 
@@ -720,8 +774,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int i = 0; i < kPBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
     for (int i = 0; i < 2 * kPBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kPEpiWarps); }
-    mbar_init(aFull, kPEpiWarps);
+    mbar_init(aFull, 1);
     mbar_init(drain, 1);
+    mbar_init(w1Full, 1);
     *sAbort = 0;
     mbar_fence_init();
   }
@@ -824,12 +879,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const float kT = p.kT;
     int T = 0, nh = 0;
     unsigned int epoch = 0;
+    uint32_t w1_use = 0;
+    const uint64_t pol_a = l2_policy_evict_last();
     bool stop = false;
     for (int k = 1; k <= n_steps && !stop; ++k) {
       for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
         // A = W1[prev] rows of this M tile (the previous MMAs on sA are done:
         // every tile of the previous tile sequence was received below)
-        {  // two threads per row: one token load, then 16 independent 16-byte loads
+        if (!kResid && k > 1) {
+          // the rows staged by the CTAs that drew the tokens of step k - 1
+          // (visible since the grid barrier): four TMA boxes of 64 K-columns
+          if (et == 0) {
+            fence_proxy_async_global();
+            mbar_expect_tx(aFull, (uint32_t)(nkc * p.box_rows * 128));
+            for (int kc = 0; kc < nkc; ++kc)
+              tma_load_3d(sA + kc * kPAChunk, &mapA, kc * 64, mt * kPM, (k - 1) & 1, aFull, pol_a);
+          }
+        } else {  // two threads per row: one token load, then 16 independent 16-byte loads each
           const int m = et >> 1, j0 = (et & 1) * 16, r = mt * kPM + m;
           int prev = -1;
           if (kResid) {
@@ -837,8 +903,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
               const int4 pd = __ldg(p.pend + r);
               prev = (pd.x == kPendResid) ? min(max(pd.z, 0), p.V - 1) : -1;
             }
-          } else if (r < p.R) {
-            prev = (k == 1) ? __ldg(p.anchor + r) : __ldcg(p.tokens + (size_t)r * p.gamma + (k - 2));
+          } else if (r < p.R) {  // k == 1: the anchors
+            prev = __ldg(p.anchor + r);
             if (prev < 0 || prev >= p.V) {
               set_status(p.status, DSPARK_ERR_RANGE);
               prev = min(max(prev, 0), p.V - 1);
@@ -854,10 +920,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int j = j0 + i, kc = j >> 3, uu = j & 7;
             *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val[i];
           }
+          fence_proxy_async_smem();
+          eg_sync();
+          if (et == 0) mbar_arrive(aFull);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(aFull);
 
         ResidRow rr{};
         if (kResid) rr = load_resid_row(p, mt * kPM + row);
@@ -957,7 +1023,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (kResid)
           locate_resid_row(p, r, sA, et);
         else
-          locate_row(p, r, k, sA, et);
+          locate_row(p, r, k, sA, et, w1Full, w1_use);
         eg_sync();
       }
       if (!kResid) {
@@ -1023,6 +1089,13 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
     if (!make_tmap_bf16(&mapBase, a.base, 3, dims, strides, box)) return cudaSuccess;
   }
   const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  CUtensorMap mapA;  // staged W1 rows [2][R][rank], one box = 64 K-columns of 128 requests
+  {
+    const uint64_t dims[3] = {(uint64_t)a.rank, (uint64_t)a.R, 2};
+    const uint64_t strides[2] = {(uint64_t)a.rank * 2, (uint64_t)a.R * a.rank * 2};
+    const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+    if (!make_tmap_bf16(&mapA, ws_at<void>(a.ws, L.astage), 3, dims, strides, box)) return cudaSuccess;
+  }
   PersistParams p;
   p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
   p.nc = ceil_div(a.V, kChunk);
@@ -1042,10 +1115,11 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   p.part = ws_at<float2>(a.ws, L.dpart);
   p.status = ws_at<uint32_t>(a.ws, L.status);
   p.gbar = reinterpret_cast<unsigned int*>(p.status + 1);
+  p.astage = ws_at<__nv_bfloat16>(a.ws, L.astage);
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapBase, &p};
+  void* args[] = {&mapW2, &mapBase, &mapA, &p};
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<false>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
@@ -1114,7 +1188,7 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapW2, &p};  // no base map in residual mode
+  void* args[] = {&mapW2, &mapW2, &mapW2, &p};  // no base or staged-row map in residual mode
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
