@@ -30,7 +30,8 @@ struct WsLayout {
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
   size_t skey0, skey1, sidx0, sidx1;  // u32 [R*gamma] radix-sort ping-pong
-  size_t fx;       // u64 [R*gamma]         fixed-point prefix sums in sorted order
+  size_t fx;       // u64 [R*gamma]         fixed-point survivals / prefix sums in sorted order
+  size_t fx2;      // u64 [R*gamma]         the same for the lagged confidences
   size_t total;
 };
 
@@ -50,6 +51,7 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.sidx0 = o;   o = align256(o + n * sizeof(uint32_t));
   L.sidx1 = o;   o = align256(o + n * sizeof(uint32_t));
   L.fx = o;      o = align256(o + n * sizeof(unsigned long long));
+  L.fx2 = o;     o = align256(o + n * sizeof(unsigned long long));
   L.total = o;
   return L;
 }

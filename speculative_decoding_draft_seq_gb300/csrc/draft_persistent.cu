@@ -857,8 +857,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
               const int stage = n % kPBStages;
               if (!mbar_wait(&bFull[stage], (n / kPBStages) & 1, sAbort, p.status)) { stop = true; break; }
               tc_fence_after();
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + kc * kPAChunk + kk * 32), 0, 1024);
+              // K rows [kc * kPKC, +kPKC): A chunk of 64 K-columns, then 32-byte K16 steps inside it
+              const unsigned char* a_k = sA + ((kc * kPKC) >> 6) * kPAChunk + (((kc * kPKC) & 63) >> 4) * 32;
+              for (int kk = 0; kk < kPKC / 16; ++kk) {
+                const uint64_t a_desc = smem_desc_sw128(smem_u32(a_k + kk * 32), 0, 1024);
                 const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * kPBStage + kk * 2048), kPBBox, 1024);
                 tc_mma_bf16(d, a_desc, b_desc, idesc, (kc | kk) != 0);
               }
@@ -890,10 +892,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
           // the rows staged by the CTAs that drew the tokens of step k - 1
           // (visible since the grid barrier): four TMA boxes of 64 K-columns
           if (et == 0) {
+            const int nka = p.rank / 64;
             fence_proxy_async_global();
-            mbar_expect_tx(aFull, (uint32_t)(nkc * p.box_rows * 128));
-            for (int kc = 0; kc < nkc; ++kc)
-              tma_load_3d(sA + kc * kPAChunk, &mapA, kc * 64, mt * kPM, (k - 1) & 1, aFull, pol_a);
+            mbar_expect_tx(aFull, (uint32_t)(nka * p.box_rows * 128));
+            for (int ka = 0; ka < nka; ++ka)
+              tma_load_3d(sA + ka * kPAChunk, &mapA, ka * 64, mt * kPM, (k - 1) & 1, aFull, pol_a);
           }
         } else {  // two threads per row: one token load, then 16 independent 16-byte loads each
           const int m = et >> 1, j0 = (et & 1) * 16, r = mt * kPM + m;
@@ -1062,13 +1065,9 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!coop || sms <= 0) return cudaSuccess;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(persistent_sweep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPSmem) != cudaSuccess)
-      return cudaSuccess;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (set_smem_limit_once((const void*)persistent_sweep_kernel<false>, (int)kPSmem, attr) != cudaSuccess)
+    return cudaSuccess;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<false>, kPThreads, kPSmem) !=
           cudaSuccess ||
@@ -1144,13 +1143,9 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!coop || sms <= 0) return cudaSuccess;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(persistent_sweep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPSmem) != cudaSuccess)
-      return cudaSuccess;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (set_smem_limit_once((const void*)persistent_sweep_kernel<true>, (int)kPSmem, attr) != cudaSuccess)
+    return cudaSuccess;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<true>, kPThreads, kPSmem) !=
           cudaSuccess ||

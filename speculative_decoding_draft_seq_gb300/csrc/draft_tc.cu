@@ -459,12 +459,10 @@ cudaError_t launch_draft_tc(const DraftArgs& a, cudaStream_t s, int& launches, b
     if (!make_tmap_bf16(&mapBase, a.base, 3, dims, strides, box)) return cudaSuccess;
   }
   taken = true;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(draft_tc_partials_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kTcSmemBytes);
+  static std::atomic<unsigned long long> attr{0};
+  {
+    cudaError_t e = set_smem_limit_once((const void*)draft_tc_partials_kernel, (int)kTcSmemBytes, attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const WsLayout L = ws_layout(a.R, a.gamma, a.V);
   TcParams p;

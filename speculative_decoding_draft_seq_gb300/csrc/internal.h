@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,6 +56,19 @@ struct VerifyArgs {
 
 // Each launcher enqueues its kernels on `s`, adds the number of kernel
 // launches to `launches`, and returns cudaGetLastError().
+// Raises a kernel's dynamic shared-memory limit, once per device (devices
+// 0..63; others every call). `done` is a per-kernel bit mask of devices.
+inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches);

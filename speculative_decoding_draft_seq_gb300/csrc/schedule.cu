@@ -18,6 +18,27 @@
 
 namespace dspark {
 
+// Coalesced copy of n words from global (L2) to shared memory with eight loads
+// in flight per thread (a load-then-store loop would wait out one memory round
+// trip per iteration).
+template <class T>
+__device__ void stage_smem(T* dst, const T* src, int n) {
+  constexpr int kU = 8;
+  for (int base = threadIdx.x; base < n; base += kU * blockDim.x) {
+    T v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int j = base + u * blockDim.x;
+      v[u] = j < n ? __ldcg(src + j) : T();
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int j = base + u * blockDim.x;
+      if (j < n) dst[j] = v[u];
+    }
+  }
+}
+
 constexpr int kSchedThreads = 1024;
 constexpr int kDigits = 16;
 // Up to this many candidates the sort keys and indices live in shared memory.
@@ -85,7 +106,7 @@ __device__ __forceinline__ double theta_of(int R, unsigned long long S, float sp
 __device__ void build_keys(const float* conf, int R, int gamma, uint32_t* key, uint32_t* idx,
                            uint32_t* stage, uint32_t* status) {
   const int n = R * gamma;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) stage[i] = __float_as_uint(__ldg(conf + i));
+  stage_smem(stage, reinterpret_cast<const uint32_t*>(conf), n);
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     float acc = 1.f;
@@ -289,23 +310,288 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small problems (R * gamma <= kRankMaxKeys): one launch of many CTAs instead
+// of one CTA.
+//
+// Every CTA forms all the survival keys in shared memory; the rank of
+// candidate i in the ascending key order (ties by flat index) is the number
+// of candidates before it, counted by kRankSplit threads over interleaved
+// slices of the keys. The rank is the candidate's position in the order the
+// radix sort gives, so sfx[rank] = fixed_point(a) lays the survivals out in
+// sorted order. The last CTA to finish (a counter in the status block, reset
+// by that CTA) runs the admission: fixed-point inclusive scan of the sorted
+// survivals, the Theta comparisons as in schedule_kernel, and
+// L_r = #{j : rank(r, j) < K} (the order is prefix-closed within a request).
+constexpr int kRankThreads = 256;
+constexpr int kRankSplit = 16;
+constexpr int kRankKeysPerCta = kRankThreads / kRankSplit;
+constexpr int kRankMaxKeys = 4096;
+constexpr size_t kSmallSmem = 2 * kRankMaxKeys * sizeof(uint32_t) + (kRankMaxKeys + 1) * sizeof(float);
+
+// The confidences are staged in `key` by one coalesced pass, then each row's
+// running product overwrites them in place.
+__device__ void survival_keys_smem(const float* conf, int R, int gamma, uint32_t* key, uint32_t* status) {
+  const int n = R * gamma;
+  stage_smem(key, reinterpret_cast<const uint32_t*>(conf), n);
+  __syncthreads();
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    float acc = 1.f;
+    for (int j = 0; j < gamma; ++j) {
+      float c = __uint_as_float(key[r * gamma + j]);
+      if (!isfinite(c)) {
+        set_status(status, DSPARK_ERR_NONFINITE);
+        c = 0.f;
+      }
+      c = c > 0.f ? fminf(c, 1.f) : 0.f;
+      acc = __fmul_rn(acc, c);
+      key[r * gamma + j] = survival_key(acc);
+    }
+  }
+}
+
+// Rank of key i among key[0..n) (ties: smaller index first); every thread of
+// the group of kRankSplit lanes that holds i gets it.
+__device__ __forceinline__ int rank_of(const uint32_t* key, int n, int i, int s) {
+  const uint32_t ki = key[min(i, n - 1)];
+  int before = 0;
+#pragma unroll 8
+  for (int j = s; j < n; j += kRankSplit) {
+    const uint32_t kj = key[j];
+    before += (kj < ki) || (kj == ki && j < i);
+  }
+#pragma unroll
+  for (int o = kRankSplit / 2; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  return before;
+}
+
+// In-place inclusive scan of v[0..n) in shared memory.
+__device__ void smem_inclusive_scan(unsigned long long* v, int n, unsigned long long* shu) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int seg = ceil_div(n, T);
+  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
+  unsigned long long loc = 0;
+  for (int i = s0; i < s1; ++i) loc += v[i];
+  unsigned long long tot;
+  unsigned long long run = block_exscan_u64(loc, shu, tot);
+  for (int i = s0; i < s1; ++i) {
+    run += v[i];
+    v[i] = run;
+  }
+  __syncthreads();
+}
+
+// Smallest argmax over the block of (value, index) pairs (float64 values).
+__device__ int block_argmax_d(double best, int besti, double* shd, int* shi) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+    if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
+  }
+  __syncthreads();
+  if (lane == 0) { shd[w] = best; shi[w] = besti; }
+  __syncthreads();
+  best = lane < nw ? shd[lane] : -INFINITY;
+  besti = lane < nw ? shi[lane] : 0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+    if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
+  }
+  __syncthreads();
+  return besti;
+}
+
+__global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
+    int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
+    const float* __restrict__ sps, int n_table, int mode, uint32_t* rank_g, unsigned long long* sfx_g,
+    unsigned long long* sfx_lag_g, int32_t* __restrict__ L, int32_t* __restrict__ Kout,
+    double* __restrict__ tau_theta, unsigned int* done, uint32_t* status) {
+  // the two key arrays, reused by the last CTA as one u64 scan array, then the
+  // cost-table window SPS[R - 1 .. R + n - 1] (dynamic shared memory)
+  extern __shared__ __align__(16) uint32_t keys[];
+  float* swin = reinterpret_cast<float*>(keys + 2 * kRankMaxKeys);
+  __shared__ unsigned long long shu[32];
+  __shared__ int shi[32];
+  __shared__ double shd[32];
+  __shared__ int sLast, sBad;
+  uint32_t* key = keys;
+  uint32_t* keyl = keys + kRankMaxKeys;
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int n = R * gamma;
+  const bool lagged = mode == DSPARK_SCHED_LAGGED;
+
+  survival_keys_smem(conf, R, gamma, key, status);
+  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, status);
+  __syncthreads();
+  const int i = blockIdx.x * kRankKeysPerCta + tid / kRankSplit;
+  const int s = tid % kRankSplit;
+  if (mode == DSPARK_SCHED_ALL) {  // no order needed: the sum is order-free
+    if (s == 0 && i < n) sfx_g[i] = fixed_point(key_survival(key[i]));
+  } else {
+    const int rk = rank_of(key, n, i, s);
+    if (s == 0 && i < n) {
+      rank_g[i] = (uint32_t)rk;
+      sfx_g[rk] = fixed_point(key_survival(key[i]));
+    }
+    if (lagged) {
+      const int rl = rank_of(keyl, n, i, s);
+      if (s == 0 && i < n) sfx_lag_g[rl] = fixed_point(key_survival(keyl[i]));
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    sLast = atomicAdd(done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!sLast) return;
+  __threadfence();
+  if (tid == 0) *done = 0u;  // ready for the next call
+
+  unsigned long long* fx = reinterpret_cast<unsigned long long*>(keys);
+  if (tid == 0) sBad = 0;
+  __syncthreads();
+  {
+    bool bad = false;
+#pragma unroll 8
+    for (int j = tid; j < n_table; j += T) bad |= !isfinite(__ldg(sps + j));
+    if (bad) sBad = 1;
+  }
+  // SPS entries R - 1 .. min(R + n, n_table) - 1, i.e. B = R .. R + n
+  const int w0 = max(R - 1, 0), w1 = min(R + n, n_table);
+  if (w1 > w0) stage_smem(swin, sps + w0, w1 - w0);
+  __syncthreads();
+  if (sBad) {
+    if (tid == 0) {
+      set_status(status, DSPARK_ERR_NONFINITE);
+      *Kout = 0;
+      tau_theta[0] = (double)R;
+      tau_theta[1] = 0.0;
+    }
+    for (int r = tid; r < R; r += T) L[r] = 0;
+    return;
+  }
+  if (mode == DSPARK_SCHED_ALL) {
+    unsigned long long loc = 0;
+    for (int j = tid; j < n; j += T) loc += __ldcg(sfx_g + j);
+    unsigned long long tot;
+    block_exscan_u64(loc, shu, tot);
+    for (int r = tid; r < R; r += T) L[r] = gamma;
+    if (tid == 0) {
+      *Kout = n;
+      tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(tot), 0x1p-40));
+      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, tot, sps[R + n - 1]) : 0.0;
+    }
+    return;
+  }
+  if (R > n_table) {
+    for (int r = tid; r < R; r += T) L[r] = 0;
+    if (tid == 0) {
+      *Kout = 0;
+      tau_theta[0] = (double)R;
+      tau_theta[1] = 0.0;
+    }
+    return;
+  }
+
+  int K = 0;
+  if (lagged) {  // K = smallest argmax of Theta_i on the lagged order, i = 0..imax
+    stage_smem(fx, sfx_lag_g, n);
+    __syncthreads();
+    smem_inclusive_scan(fx, n, shu);
+    const int imax = min(n, n_table - R);
+    double best = -INFINITY;
+    int besti = 0x7fffffff;
+    for (int j = tid; j <= imax; j += T) {
+      const double th = theta_of(R, j ? fx[j - 1] : 0ull, swin[R + j - 1 - w0]);
+      if (th > best || (th == best && j < besti)) { best = th; besti = j; }
+    }
+    K = block_argmax_d(best, besti, shd, shi);
+  }
+
+  stage_smem(fx, sfx_g, n);
+  __syncthreads();
+  smem_inclusive_scan(fx, n, shu);
+
+  if (mode == DSPARK_SCHED_CAUSAL) {  // the first admission that would lower Theta stops
+    int stop = 0x7fffffff;
+    for (int j = tid; j < n; j += T) {
+      const int B = R + j + 1;
+      bool st = B > n_table;
+      if (!st) {
+        const double th_next = theta_of(R, fx[j], swin[B - 1 - w0]);
+        const double th_prev = theta_of(R, j ? fx[j - 1] : 0ull, swin[B - 2 - w0]);
+        st = th_next < th_prev;
+      }
+      if (st) {
+        stop = j;
+        break;
+      }
+    }
+    K = block_min_i(stop, shi);
+    if (K == 0x7fffffff) K = n;
+  }
+  if (tid == 0) {
+    const unsigned long long S = K ? fx[K - 1] : 0ull;
+    *Kout = K;
+    tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
+    tau_theta[1] = theta_of(R, S, swin[R + K - 1 - w0]);
+  }
+  uint32_t* srank = keys;  // the ranks, staged over the scan array
+  __syncthreads();
+  stage_smem(srank, rank_g, n);
+  __syncthreads();
+  for (int r = tid; r < R; r += T) {
+    int cnt = 0;
+    for (int j = 0; j < gamma; ++j) cnt += srank[r * gamma + j] < (uint32_t)K;
+    L[r] = cnt;
+  }
+}
+
+// Both scheduler forms behind one call: the many-CTA rank kernel (admission
+// in its last CTA) for small problems, the single-CTA radix sort otherwise.
+// Scratch: key0/key1/idx0/idx1 (u32[n] each), fx (u64[n]), for the small form
+// fx2 (u64[n]); status[0] is the sticky status word and status[2] the small
+// form's completion counter (zero between calls).
+cudaError_t schedule_launch(const ScheduleArgs& a, uint32_t* key0, uint32_t* key1, uint32_t* idx0, uint32_t* idx1,
+                            unsigned long long* fx, unsigned long long* fx2, uint32_t* status, cudaStream_t s,
+                            int& launches) {
+  const long long n = (long long)a.R * a.gamma;
+  if (n <= kRankMaxKeys) {
+    const int grid = (int)ceil_div(n, kRankKeysPerCta);
+    static std::atomic<unsigned long long> attr{0};
+    {
+      cudaError_t e = set_smem_limit_once((const void*)schedule_small_kernel, (int)kSmallSmem, attr);
+      if (e != cudaSuccess) return e;
+    }
+    schedule_small_kernel<<<grid, kRankThreads, kSmallSmem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table,
+                                                        a.mode, key0, fx, fx2, a.sched_len, a.K, a.tau_theta,
+                                                        status + 2, status);
+    launches += 1;
+    return cudaGetLastError();
+  }
+  const size_t smem = kCntBytes + (n <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
+  static std::atomic<unsigned long long> attr{0};
+  {
+    cudaError_t e = set_smem_limit_once((const void*)schedule_kernel, (int)kSchedSmemMax, attr);
+    if (e != cudaSuccess) return e;
+  }
+  schedule_kernel<<<1, kSchedThreads, smem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table, a.mode,
+                                                 a.sched_len, a.K, a.tau_theta, key0, key1, idx0, idx1, fx, status);
+  launches += 1;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches) {
   const WsLayout L = ws_layout(a.R, a.gamma, 1);
   void* ws = a.ws;
-  const size_t smem = kCntBytes + ((long long)a.R * a.gamma <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSchedSmemMax);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  schedule_kernel<<<1, kSchedThreads, smem, s>>>(
-      a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table, a.mode, a.sched_len, a.K, a.tau_theta,
-      ws_at<uint32_t>(ws, L.skey0), ws_at<uint32_t>(ws, L.skey1), ws_at<uint32_t>(ws, L.sidx0),
-      ws_at<uint32_t>(ws, L.sidx1), ws_at<unsigned long long>(ws, L.fx), ws_at<uint32_t>(ws, L.status));
-  launches += 1;
-  return cudaGetLastError();
+  return schedule_launch(a, ws_at<uint32_t>(ws, L.skey0), ws_at<uint32_t>(ws, L.skey1), ws_at<uint32_t>(ws, L.sidx0),
+                         ws_at<uint32_t>(ws, L.sidx1), ws_at<unsigned long long>(ws, L.fx),
+                         ws_at<unsigned long long>(ws, L.fx2), ws_at<uint32_t>(ws, L.status), s, launches);
 }
 
 }  // namespace dspark
@@ -335,7 +621,6 @@ static __device__ __align__(256) unsigned char g_schedule_scratch[kStaticScratch
 
 constexpr int kStaticMaxDevices = 64;
 static void* g_schedule_scratch_ptr[kStaticMaxDevices] = {};
-static bool g_schedule_static_attr[kStaticMaxDevices] = {};
 
 }  // namespace dspark
 
@@ -359,24 +644,26 @@ extern "C" dspark_status dspark_schedule_static(int32_t R, int32_t gamma, const 
     if (cudaGetSymbolAddress(&p, g_schedule_scratch) != cudaSuccess || p == nullptr) return DSPARK_ERR_CUDA;
     g_schedule_scratch_ptr[dev] = p;
   }
-  const size_t smem = kCntBytes + ((long long)R * gamma <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
-  if (!g_schedule_static_attr[dev]) {
-    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSchedSmemMax) !=
-        cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    g_schedule_static_attr[dev] = true;
-  }
   char* base = static_cast<char*>(g_schedule_scratch_ptr[dev]);
   uint32_t* status = reinterpret_cast<uint32_t*>(base + kStaticStatusOff);
   cudaStream_t s = (cudaStream_t)stream;
   // The status word is the only scratch that must start at zero; every other
   // byte a call reads it has written first.
   if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return DSPARK_ERR_CUDA;
-  schedule_kernel<<<1, kSchedThreads, smem, s>>>(
-      R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta,
-      reinterpret_cast<uint32_t*>(base + kStaticKey0Off), reinterpret_cast<uint32_t*>(base + kStaticKey1Off),
-      reinterpret_cast<uint32_t*>(base + kStaticIdx0Off), reinterpret_cast<uint32_t*>(base + kStaticIdx1Off),
-      reinterpret_cast<unsigned long long*>(base + kStaticFxOff), status);
+  // the small form's second survival array shares the key0/key1 bytes, which
+  // that form leaves unused (it keeps its ranks in idx0)
+  const ScheduleArgs a{R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta, nullptr};
+  int launches = 0;
+  const bool small = (long long)R * gamma <= kRankMaxKeys;
+  uint32_t* key0 = reinterpret_cast<uint32_t*>(base + kStaticKey0Off);
+  uint32_t* key1 = reinterpret_cast<uint32_t*>(base + kStaticKey1Off);
+  uint32_t* idx0 = reinterpret_cast<uint32_t*>(base + kStaticIdx0Off);
+  uint32_t* idx1 = reinterpret_cast<uint32_t*>(base + kStaticIdx1Off);
+  if (schedule_launch(a, small ? idx0 : key0, key1, small ? key0 : idx0, idx1,
+                      reinterpret_cast<unsigned long long*>(base + kStaticFxOff),
+                      reinterpret_cast<unsigned long long*>(base + kStaticKey0Off), status, s,
+                      launches) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   if (device_status != nullptr &&
       cudaMemcpyAsync(device_status, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

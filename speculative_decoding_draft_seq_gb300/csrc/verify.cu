@@ -139,33 +139,45 @@ __global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
   }
 }
 
-__global__ void verify_chain_kernel(int R, int gamma, const int32_t* __restrict__ tokens,
-                                    const int32_t* __restrict__ anchor, const float* __restrict__ q_tok,
-                                    const int32_t* __restrict__ sched_len, uint64_t seed, int greedy,
-                                    const float4* __restrict__ rowstat, float* __restrict__ p_tok,
-                                    int32_t* __restrict__ out, int32_t* __restrict__ acc_len,
-                                    int4* __restrict__ pend) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= R) return;
+__global__ void __launch_bounds__(256) verify_chain_kernel(
+    int R, int gamma, const int32_t* __restrict__ tokens, const int32_t* __restrict__ anchor,
+    const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len, uint64_t seed, int greedy,
+    const float4* __restrict__ rowstat, float* __restrict__ p_tok, int32_t* __restrict__ out,
+    int32_t* __restrict__ acc_len, int4* __restrict__ pend) {
+  // one warp per request; lane l tests positions k = l + 1, l + 33, ... at once
+  const int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (r >= R) return;  // whole warps
   const int L = min(max(sched_len[r], 0), gamma);
   int A = L;
-  for (int k = 1; k <= L; ++k) {
-    const float p = p_tok[(size_t)r * gamma + k - 1];
-    const float q = q_tok[(size_t)r * gamma + k - 1];
-    const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)k, kAccept);
-    const bool ok = (q <= 0.f) || (u < (double)p / (double)q);
-    if (!ok) { A = k - 1; break; }
+  for (int k0 = 1; k0 <= L; k0 += 32) {
+    const int k = k0 + lane;
+    bool fail = false;
+    if (k <= L) {
+      const float p = p_tok[(size_t)r * gamma + k - 1];
+      const float q = q_tok[(size_t)r * gamma + k - 1];
+      const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)k, kAccept);
+      fail = !((q <= 0.f) || (u < (double)p / (double)q));
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, fail);
+    if (m) {  // the first rejected position k0 + ffs - 1 keeps A = k - 1 tokens
+      A = k0 + __ffs(m) - 2;
+      break;
+    }
   }
-  acc_len[r] = A;
-  for (int k = 0; k < A; ++k) out[(size_t)r * (gamma + 1) + k] = tokens[(size_t)r * gamma + k];
-  for (int k = A + 1; k <= gamma; ++k) out[(size_t)r * (gamma + 1) + k] = -1;
-  for (int k = L; k < gamma; ++k) p_tok[(size_t)r * gamma + k] = 0.f;
-  const int prev = A ? tokens[(size_t)r * gamma + A - 1] : anchor[r];
-  if (greedy) {
-    out[(size_t)r * (gamma + 1) + A] = __float_as_int(rowstat[(size_t)r * (gamma + 1) + A].z);
-    pend[r] = make_int4(kPendNone, A, prev, A);
-  } else {
-    pend[r] = make_int4(A < L ? kPendResid : kPendBonus, A, prev, A);
+  for (int k = lane; k <= gamma; k += 32) {
+    if (k < A) out[(size_t)r * (gamma + 1) + k] = tokens[(size_t)r * gamma + k];
+    else if (k > A) out[(size_t)r * (gamma + 1) + k] = -1;
+    if (k >= L && k < gamma) p_tok[(size_t)r * gamma + k] = 0.f;
+  }
+  if (lane == 0) {
+    acc_len[r] = A;
+    const int prev = A ? tokens[(size_t)r * gamma + A - 1] : anchor[r];
+    if (greedy) {
+      out[(size_t)r * (gamma + 1) + A] = __float_as_int(rowstat[(size_t)r * (gamma + 1) + A].z);
+      pend[r] = make_int4(kPendNone, A, prev, A);
+    } else {
+      pend[r] = make_int4(A < L ? kPendResid : kPendBonus, A, prev, A);
+    }
   }
 }
 
@@ -357,7 +369,7 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
   const Tin* W2 = static_cast<const Tin*>(a.W2);
   verify_stats_kernel<Tin><<<dim3(a.R, a.gamma + 1), kStatThreads, 0, s>>>(
       a.R, a.gamma, a.V, target, a.tokens, a.sched_len, kT, greedy, rowstat, a.p_tok, status);
-  verify_chain_kernel<<<ceil_div(a.R, 128), 128, 0, s>>>(a.R, a.gamma, a.tokens, a.anchor, a.q_tok,
+  verify_chain_kernel<<<ceil_div(a.R, 8), 256, 0, s>>>(a.R, a.gamma, a.tokens, a.anchor, a.q_tok,
                                                           a.sched_len, a.seed, greedy, rowstat, a.p_tok,
                                                           a.out_tokens, a.accepted_len, pend);
   launches += 2;
