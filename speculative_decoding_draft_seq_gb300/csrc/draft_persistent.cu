@@ -525,45 +525,97 @@ __device__ __forceinline__ float unpack_bf16(const uint4& x, int e) {
   return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
 }
 
-// Epilogue of the residual pass for one 64-column chunk of one request: the
-// bias comes from TMEM (two warp-collective loads), the target and base rows
-// of the request's own position A from global memory.
-__device__ __forceinline__ void resid_chunk(const PersistParams& p, const ResidRow& rr, int r, int vbase,
-                                            uint32_t taddr, float& sw, float& sp) {
-  const bool act = rr.kind != kPendNone;
-  uint4 tb[8], bb[8];
+// Residual-pass staging of the target and base rows. Each epilogue warp owns
+// 32 requests (its TMEM lane quarter) and a 12 KB slice of the staging region
+// (the base ring and the third W2 stage of the drafting layout): three
+// buffers of one half-chunk (32 columns) of both rows,
+// 32 rows x 64 bytes per tensor, the 16-byte unit u of row m stored at
+// m * 64 + ((u ^ ((m >> 1) & 3)) << 4) so the per-row reads are free of bank
+// conflicts. The copies are cp.async (16 bytes each), four per tensor and
+// lane, laid out so consecutive lanes read consecutive 16 bytes of one row;
+// rows without a pending draw, base rows of bonus draws and columns past V are
+// zero-filled without reading global memory.
+constexpr int kRsBufs = 3;  // ring of half-chunk buffers per warp: copies run two ahead
+constexpr uint32_t kRsBufBytes = 4096;
+constexpr uint32_t kRsWarpBytes = kRsBufs * kRsBufBytes;
+constexpr uint32_t kRsTensorBytes = 2048;
+static_assert(2 * kPBStage + kPEpiWarps * kRsWarpBytes <= kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox,
+              "the residual layout (2 W2 stages + row staging) fits where the drafting layout keeps 3 stages "
+              "and the base ring");
+
+struct ResidCopyRows {  // per lane: global rows of the four (copy, row) slots it serves
+  int trow[4], brow[4];   // -1: zero fill
+};
+
+__device__ __forceinline__ ResidCopyRows resid_copy_rows(const PersistParams& p, const ResidRow& rr, int r, int lane) {
+  const int my_t = rr.kind != kPendNone ? r * (p.gamma + 1) + rr.A : -1;
+  const int my_b = rr.kind == kPendResid ? r * p.gamma + min(rr.A, p.gamma - 1) : -1;
+  ResidCopyRows cr;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { tb[i] = make_uint4(0, 0, 0, 0); bb[i] = make_uint4(0, 0, 0, 0); }
-  if (act) {
-    const uint4* tp = reinterpret_cast<const uint4*>(p.target + ((size_t)r * (p.gamma + 1) + rr.A) * p.V + vbase);
-    const uint4* bp = reinterpret_cast<const uint4*>(p.base + ((size_t)r * p.gamma + min(rr.A, p.gamma - 1)) * p.V + vbase);
+  for (int c = 0; c < 4; ++c) {
+    const int src = c * 8 + (lane >> 2);
+    cr.trow[c] = __shfl_sync(0xffffffffu, my_t, src);
+    cr.brow[c] = __shfl_sync(0xffffffffu, my_b, src);
+  }
+  return cr;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Issues the copies of one half-chunk (columns [v0, v0 + 32)) into `buf`, and
+// commits them as one group (an empty group when v0 < 0).
+__device__ __forceinline__ void resid_issue(const PersistParams& p, const ResidCopyRows& cr, int v0, int lane,
+                                            uint32_t buf) {
+  if (v0 >= 0) {
+    const int u = lane & 3;
+    const int v = v0 + 8 * u;
+    const bool in = v < p.V;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (vbase + 8 * i < p.V) {
-        tb[i] = __ldg(tp + i);
-        if (rr.kind == kPendResid) bb[i] = __ldg(bp + i);
-      }
+    for (int c = 0; c < 4; ++c) {
+      const int m = c * 8 + (lane >> 2);
+      const uint32_t off = (uint32_t)(m * 64 + ((u ^ ((m >> 1) & 3)) << 4));
+      const int tr = cr.trow[c], br = cr.brow[c];
+      const __nv_bfloat16* ts = p.target + (size_t)max(tr, 0) * p.V + (in ? v : 0);
+      const __nv_bfloat16* bs = p.base + (size_t)max(br, 0) * p.V + (in ? v : 0);
+      cp_async16(buf + off, ts, (in && tr >= 0) ? 16u : 0u);
+      cp_async16(buf + kRsTensorBytes + off, bs, (in && br >= 0) ? 16u : 0u);
     }
   }
-  sw = 0.f;
-  sp = 0.f;
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Residual weights of one half-chunk of row m: the bias from TMEM (32
+// columns), the target and base values from the staged buffer. Branch-free
+// per element (residual and bonus rows share a warp): for a bonus draw Q is
+// formed against a maximum of +inf, so it is exactly 0 and max(0, P - Q) = P,
+// the same value resid_w returns; columns past V are masked to 0.
+__device__ __forceinline__ void resid_half(const PersistParams& p, const ResidRow& rr, int v0, uint32_t taddr,
+                                           const unsigned char* buf, int m, float (&sw)[4], float (&sp)[4]) {
+  float acc[32];
+  __syncwarp();
+  tmem_ld32(taddr, acc);
+  if (rr.kind == kPendNone) return;
+  const bool res = rr.kind == kPendResid;
+  const float kT = p.kT, MPk = rr.MPk, invZP = rr.invZP;
+  const float MQk = res ? rr.MQk : INFINITY, invZQ = res ? rr.invZQ : 0.f;
+  const int nvalid = p.V - v0;  // columns col < nvalid exist
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float acc[32];
-    __syncwarp();
-    tmem_ld32(taddr + (uint32_t)(half * 32), acc);
-    if (act) {
+  for (int u = 0; u < 4; ++u) {  // unit u feeds accumulator pair u: four independent chains
+    const uint32_t off = (uint32_t)(m * 64 + ((u ^ ((m >> 1) & 3)) << 4));
+    const uint4 tv = *reinterpret_cast<const uint4*>(buf + off);
+    const uint4 bv = *reinterpret_cast<const uint4*>(buf + kRsTensorBytes + off);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int col = half * 32 + i;
-        if (vbase + col < p.V) {
-          const float t = unpack_bf16(tb[col >> 3], col & 7);
-          const float l = __fadd_rn(unpack_bf16(bb[col >> 3], col & 7), acc[i]);
-          float P;
-          sw += resid_w(rr.kind, t, l, rr, p.kT, P);
-          sp += P;
-        }
-      }
+    for (int e = 0; e < 8; ++e) {
+      const int col = 8 * u + e;
+      const float t = unpack_bf16(tv, e);
+      const float l = __fadd_rn(unpack_bf16(bv, e), acc[col]);
+      const float P = __fmul_rn(pweight(t, kT, MPk), invZP);
+      const float Q = __fmul_rn(pweight(l, kT, MQk), invZQ);
+      const bool in = col < nvalid;
+      sw[u] += in ? fmaxf(0.f, __fsub_rn(P, Q)) : 0.f;
+      sp[u] += in ? P : 0.f;
     }
   }
 }
@@ -746,10 +798,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             const __grid_constant__ CUtensorMap mapA, PersistParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // drafting: A | 3 W2 stages | base ring; residual pass: A | 2 W2 stages |
+  // row staging (the W2 ring gives up a stage to keep more rows in flight)
+  constexpr int kBStages = kResid ? 2 : kPBStages;
   unsigned char* sA = smem;
   unsigned char* sB = sA + kPABytes;
-  unsigned char* sBase = sB + kPBStages * kPBStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + 2 * kPBaseStages * kPBaseBox);
+  unsigned char* sBase = sB + kBStages * kPBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + kPABytes + kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox);
   uint64_t* bFull = bars;
   uint64_t* bEmpty = bFull + kPBStages;
   uint64_t* baseFull = bEmpty + kPBStages;          // [half][stage]
@@ -800,16 +855,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int t = 0; t < n_tiles && !stop; ++t) {
             const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
             for (int kc = 0; kc < nkc; ++kc) {
-              const int stage = n % kPBStages;
-              if (!mbar_wait(&bEmpty[stage], ((n / kPBStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+              const int stage = n % kBStages;
+              if (!mbar_wait(&bEmpty[stage], ((n / kBStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
               mbar_expect_tx(&bFull[stage], nbox * kPBBox);
               for (int j = 0; j < nbox; ++j)
                 tma_load_2d(sB + stage * kPBStage + j * kPBBox, &mapW2, (c0 + j) * 64, kc * kPKC, &bFull[stage], pol);
               ++n;
             }
           }
-      for (int i = 1; i <= kPBStages && n - i >= 0; ++i)
-        mbar_wait_drain(&bFull[(n - i) % kPBStages], ((n - i) / kPBStages) & 1, p.status);
+      for (int i = 1; i <= kBStages && n - i >= 0; ++i)
+        mbar_wait_drain(&bFull[(n - i) % kBStages], ((n - i) / kBStages) & 1, p.status);
     }
   } else if (warp == 2) {
     if (!kResid && lane == 0) {  // base-logit producer: chunk j of a tile -> ring of half j & 1
@@ -854,8 +909,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t idesc = idesc_bf16_f32(kPM, (uint32_t)(64 * nbox), 1);
             const uint32_t d = tmem + (uint32_t)(buf * 256);
             for (int kc = 0; kc < nkc; ++kc, ++n) {
-              const int stage = n % kPBStages;
-              if (!mbar_wait(&bFull[stage], (n / kPBStages) & 1, sAbort, p.status)) { stop = true; break; }
+              const int stage = n % kBStages;
+              if (!mbar_wait(&bFull[stage], (n / kBStages) & 1, sAbort, p.status)) { stop = true; break; }
               tc_fence_after();
               // K rows [kc * kPKC, +kPKC): A chunk of 64 K-columns, then 32-byte K16 steps inside it
               const unsigned char* a_k = sA + ((kc * kPKC) >> 6) * kPAChunk + (((kc * kPKC) & 63) >> 4) * 32;
@@ -929,7 +984,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
 
         ResidRow rr{};
-        if (kResid) rr = load_resid_row(p, mt * kPM + row);
+        ResidCopyRows cr{};
+        // residual pass: this warp's half-chunk sequence s = 0, 1, ...: chunk
+        // kth = s >> 1 of this half (c_begin + 4 (kth >> 1) + h + 2 (kth & 1)),
+        // columns 32 (s & 1) .. +32; copies run one half-chunk ahead
+        const uint32_t rs_base = smem_u32(sBase) + (uint32_t)ew * kRsWarpBytes;
+        auto hc_col = [&](int sidx) -> int {
+          const int kth = sidx >> 1, c = c_begin + 4 * (kth >> 1) + h + 2 * (kth & 1);
+          return c < c_end ? c * 64 + 32 * (sidx & 1) : -1;
+        };
+        int hs = 0;
+        if (kResid) {
+          __syncwarp();  // the previous M tile's reads of the buffers are done
+          rr = load_resid_row(p, mt * kPM + row);
+          cr = resid_copy_rows(p, rr, mt * kPM + row, lane);
+          resid_issue(p, cr, hc_col(0), lane, rs_base);
+          resid_issue(p, cr, hc_col(1), lane, rs_base + kRsBufBytes);
+        }
         for (int t = 0; t < n_tiles; ++t, ++T) {
           const int buf = T & 1;
           const uint32_t use = (uint32_t)(T >> 1);
@@ -939,10 +1010,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int j = h; j < nbox; j += 2) {
             if (kResid) {
               const int r = mt * kPM + row;
-              float sw, sp;
-              resid_chunk(p, rr, r, (c0 + j) * 64,
-                          tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), sw, sp);
-              if (rr.kind != kPendNone) __stcg(p.rpart + (size_t)r * p.nc + (c0 + j), make_float2(sw, sp));
+              float sw[4] = {0.f, 0.f, 0.f, 0.f}, sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+              for (int hh = 0; hh < 2; ++hh, ++hs) {
+                __syncwarp();  // every lane is done with the buffer the next copies overwrite
+                resid_issue(p, cr, hc_col(hs + 2), lane, rs_base + (uint32_t)((hs + 2) % kRsBufs) * kRsBufBytes);
+                asm volatile("cp.async.wait_group 2;" ::: "memory");
+                __syncwarp();
+                resid_half(p, rr, (c0 + j) * 64 + 32 * hh,
+                           tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh),
+                           sBase + (size_t)ew * kRsWarpBytes + (size_t)(hs % kRsBufs) * kRsBufBytes, lane, sw, sp);
+              }
+              if (rr.kind != kPendNone)
+                __stcg(p.rpart + (size_t)r * p.nc + (c0 + j),
+                       make_float2((sw[0] + sw[1]) + (sw[2] + sw[3]), (sp[0] + sp[1]) + (sp[2] + sp[3])));
               continue;
             }
             const int s = h * kPBaseStages + nh % kPBaseStages;
@@ -986,14 +1067,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int i = 0; i < 32; ++i)
                   if (l[i] > m) { m = l[i]; am = vh + i; }
               } else {
-                float mh = l[0];
+                // four independent chains (the max is exact in any order;
+                // the sum is a float32 chunk partial either way)
+                float mq[4] = {l[0], l[1], l[2], l[3]};
 #pragma unroll
-                for (int i = 1; i < 32; ++i) mh = fmaxf(mh, l[i]);
-                const float mn = fmaxf(m, mh);
+                for (int i = 4; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], l[i]);
+                const float mn = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
                 const float mk = __fmul_rn(mn, kT);
-                float sh = 0.f;
+                float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sh += pweight(l[i], kT, mk);
+                for (int i = 0; i < 32; ++i) sq[i & 3] += pweight(l[i], kT, mk);
+                const float sh = (sq[0] + sq[1]) + (sq[2] + sq[3]);
                 ssum = (m == -INFINITY ? 0.f : ssum * pweight(m, kT, mk)) + sh;
                 m = mn;
               }
@@ -1039,6 +1123,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (*sDecide) break;
       }
     }
+    if (kResid) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
     *sAbort = (*sAbort) | (stop ? 1 : 0);  // let the other roles wind down
     (void)ew;
   }
