@@ -48,27 +48,38 @@ def algorithmic_bytes(cfg, L):
     return draft, verify
 
 
-def cpu_baseline(cfg, n_req, timeout=600):
-    """Times the oracle on `n_req` requests in a single-threaded child process."""
+def cpu_baseline(cfg, n_req, steps=1, warmup=0, timeout=900):
+    """Times the oracle in one single-threaded child process: `warmup` untimed
+    and `steps` timed steps, each a full round over all requests' schedule with
+    draft + verify of `n_req` requests (a different sample every step)."""
     code = (
         "import time, json, sys; sys.path.insert(0, %r)\n"
         "import workloads as W\n"
         "from oracle.round import run_round\n"
         "cfg = W.CONFIGS[%r]\n"
-        "req = list(range(%d))\n"
-        "inp = W.oracle_inputs(cfg, req)\n"
-        "t = time.perf_counter(); run_round(inp, requests=req); dt = time.perf_counter() - t\n"
-        "print(json.dumps({'seconds': dt}))\n" % (ROOT, cfg.name, n_req))
+        "n, steps, warm = %d, %d, %d\n"
+        "pool = min(cfg.R, max(n, 8))\n"
+        "reqs = [[(i * n + j) %% pool for j in range(n)] for i in range(steps + warm)]\n"
+        "allr = sorted(set(r for q in reqs for r in q))\n"
+        "inp = W.oracle_inputs(cfg, allr)\n"
+        "ts = []\n"
+        "for i, q in enumerate(reqs):\n"
+        "    t = time.perf_counter(); run_round(inp, requests=q); dt = time.perf_counter() - t\n"
+        "    if i >= warm: ts.append(dt)\n"
+        "print(json.dumps({'seconds': ts}))\n" % (ROOT, cfg.name, n_req, steps, warmup))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                          timeout=timeout)
     if out.returncode != 0:
         raise RuntimeError(out.stderr[-2000:])
-    dt = json.loads(out.stdout.strip().splitlines()[-1])["seconds"]
-    pos = n_req * cfg.gamma
+    ts = json.loads(out.stdout.strip().splitlines()[-1])["seconds"]
+    dt = float(sum(ts))
+    pos = n_req * cfg.gamma * len(ts)
     return {"value": pos / dt, "unit": "positions/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_req} of {cfg.R} requests x gamma={cfg.gamma} (full round: schedule over all "
-                      f"requests, draft + verify of the sampled ones), single thread, {dt:.1f} s"}
+            "sample": f"{len(ts)} step(s) of {n_req} of {cfg.R} requests x gamma={cfg.gamma} (drawn from the "
+                      f"first {min(cfg.R, max(n_req, 8))}; each a full round: "
+                      f"schedule over all requests, draft + verify of the sampled ones), single thread, "
+                      f"{dt:.1f} s timed"}
 
 
 class ClockSampler:
@@ -90,6 +101,14 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        # nvidia-smi needs a moment before its first line: wait for it (at most
+        # 5 s) so that the samples cover the timed region that follows
+        t0 = time.time()
+        while time.time() - t0 < 5.0:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -115,22 +134,57 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# DRAM bytes per launch of the persistent drafting / residual kernel, from
+# one ncu capture of the full-size round (profiles/traffic_ds_round.md). The
+# figure stands only while the CUDA sources are the ones it was taken on.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_ds_round.md")
+
+
+def csrc_digest():
+    import hashlib
+    d = os.path.join(ROOT, "speculative_decoding_draft_seq_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel):
+    key = {"draft": "traffic.draft", "verify": "traffic.verify_resid"}[kernel]
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    vals = dict(l.split()[:2] for l in lines if len(l.split()) >= 2 and l.split()[0].startswith(("traffic.", "sources")))
+    if vals.get("sources") != csrc_digest() or key not in vals:
+        return None
+    return int(vals[key])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="ds")
     ap.add_argument("--temperature", type=float, default=None)
     ap.add_argument("--cpu-requests", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
+    ap.add_argument("--profile", choices=["round", "draft"], default=None,
+                    help="launch only, for an ncu capture: 'round' = one round then two verify calls, "
+                         "'draft' = three drafting calls; prints the device status")
     args = ap.parse_args()
 
     import workloads as W
     cfg = W.CONFIGS[args.config]
     if args.temperature is not None:
         cfg = W.with_(cfg, T=args.temperature)
+    if args.gamma is not None:
+        cfg = W.with_(cfg, gamma=args.gamma)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     workload = (f"{cfg.name}: R={cfg.R} gamma={cfg.gamma} V={cfg.V} rank={cfg.rank} {cfg.dtype} "
@@ -139,18 +193,17 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        ref_steps = []
-        for _ in range(max(1, args.steps)):
-            b = cpu_baseline(cfg, max(1, args.cpu_requests // 4))
-            ref_steps.append(b)
-        v = sum(x["value"] for x in ref_steps) / len(ref_steps)
+        # one request per step: the oracle takes about a quarter of a second per
+        # DeepSeek-scale request, so the default 300 steps stay within minutes
+        b = cpu_baseline(cfg, 1, steps=max(1, args.steps), warmup=args.warmup)
+        v = b["value"]
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "positions/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * cfg.R * cfg.gamma / v, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": workload},
                 "cpu_baseline": {"value": v, "unit": "positions/s", "cores": 1, "kind": "oracle",
-                                 "sample": ref_steps[0]["sample"]},
+                                 "sample": b["sample"]},
                 "e2e": {"value": v, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -173,6 +226,24 @@ def main():
     ws = dspark.new_workspace(R, gamma, V, cfg.rank, dt_code, cfg.n_table, dev)
     out = dspark.RoundOutputs(R, gamma, dev)
     stream = torch.cuda.current_stream()
+    if args.profile:
+        if args.profile == "round":
+            dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                          inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+            for _ in range(2):
+                dspark.verify(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], out.tokens,
+                              out.q_tok, out.q_stats, out.sched_len, inp["T"], inp["seed"], out.out_tokens,
+                              out.accepted_len, out.p_tok, ws)
+        else:
+            for _ in range(3):
+                dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"],
+                                        out.tokens, out.q_tok, out.q_stats, ws)
+        torch.cuda.synchronize()
+        st = dspark.device_status(ws)
+        print(json.dumps({"profile": args.profile, "workload": workload, "status": dspark.status_string(st)}))
+        if st != dspark.OK:
+            sys.exit(1)
+        return
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def one_round():
@@ -276,7 +347,7 @@ def main():
     verify_gbs = bv / (t_verify * 1e-3) / 1e9
     dominant = "draft" if t_draft >= t_verify else "verify"
     ach = draft_gbs if dominant == "draft" else verify_gbs
-    traffic = None
+    traffic = measured_traffic(dominant)
     line = {
         "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
