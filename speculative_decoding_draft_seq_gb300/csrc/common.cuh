@@ -104,18 +104,10 @@ __device__ __forceinline__ unsigned long long scale_u53(uint64_t odd53, unsigned
   return (hi << 11) | (lo >> 53);
 }
 
-// floor(f * 2^40) for a finite float f >= 0, exactly, with integer operations
-// (values below 2^-40 give 0). Masses up to 2^23 fit without overflow.
-__device__ __forceinline__ unsigned long long fx40(float f) {
-  const uint32_t b = __float_as_uint(f);
-  const int e = (int)((b >> 23) & 0xFFu);
-  if (e == 0 || (b >> 31)) return 0ull;
-  const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
-  const int sh = e - 127 - 23 + 40;
-  if (sh >= 0) return m << sh;
-  if (sh <= -24) return 0ull;
-  return m >> (-sh);
-}
+// floor(f * 2^40) for a float f: f * 2^40 is exact in float32 (a power-of-two
+// scaling, no overflow below 2^88), and the truncating conversion to u64 is
+// the floor for f >= 0; negative, NaN and subnormal-range inputs give 0.
+__device__ __forceinline__ unsigned long long fx40(float f) { return __float2ull_rz(__fmul_rn(f, 0x1p40f)); }
 
 __device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t r, uint64_t k, uint64_t purpose) {
   return (double)philox_odd53(seed, r, k, purpose) * 0x1p-53;

@@ -325,14 +325,14 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   // summed exactly as 2^-40 fixed-point integers
   unsigned long long local = 0ull;
   int last_pos = -1;
+  unsigned long long fmass[kCache];  // this thread's chunk masses, reused by the crossing search
   if (cached) {
 #pragma unroll
-    for (int i = 0; i < kCache; ++i)
-      if (i < c1 - c0) {
-        const unsigned long long f = fx40(__fmul_rn(cache[i].y, pweight(cache[i].x, kT, Mk)));
-        if (f) last_pos = c0 + i;
-        local += f;
-      }
+    for (int i = 0; i < kCache; ++i) {
+      fmass[i] = i < c1 - c0 ? fx40(__fmul_rn(cache[i].y, pweight(cache[i].x, kT, Mk))) : 0ull;
+      if (fmass[i]) last_pos = c0 + i;
+      local += fmass[i];
+    }
   } else {
     for (int c = c0; c < c1; ++c) {
       const float2 q = __ldcg(pr + c);
@@ -358,14 +358,20 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     int found = -1;
     float found_g = 0.f, found_m = 0.f;
     if (cached) {
+      int fi = -1;
 #pragma unroll
-      for (int i = 0; i < kCache; ++i)
-        if (i < c1 - c0) {
-          const float g = pweight(cache[i].x, kT, Mk);
-          const unsigned long long f = fx40(__fmul_rn(cache[i].y, g));
-          if (found < 0 && run + f > target) { found = c0 + i; found_excl = run; found_g = g; found_m = cache[i].x; }
-          run += f;
-        }
+      for (int i = 0; i < kCache; ++i) {
+        if (fi < 0 && run + fmass[i] > target) { fi = i; found_excl = run; }
+        run += fmass[i];
+      }
+      if (fi >= 0) {
+        found = c0 + fi;
+        float mq = 0.f;
+#pragma unroll
+        for (int i = 0; i < kCache; ++i) mq = i == fi ? cache[i].x : mq;  // static indexing
+        found_g = pweight(mq, kT, Mk);
+        found_m = mq;
+      }
     } else {
       for (int c = c0; c < c1 && found < 0; ++c) {
         const float2 q = __ldcg(pr + c);
