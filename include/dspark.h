@@ -83,10 +83,10 @@ typedef enum {
 size_t dspark_workspace_bytes(int32_t R, int32_t gamma, int32_t V, int32_t rank,
                               int32_t dtype, int32_t n_table);
 
-/* Clears the workspace's status block (async on `stream`): the sticky status
- * word and the library's internal counters. Call once after allocating a
- * workspace; every entry point below leaves earlier errors in place (sticky)
- * until this is called again. */
+/* Clears the whole workspace (async on `stream`): the sticky status word and
+ * the library's internal completion counters, which every call leaves at zero
+ * again. Call once after allocating a workspace; every entry point below
+ * leaves earlier errors in place (sticky) until this is called again. */
 dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes,
                                     dspark_stream_t stream);
 

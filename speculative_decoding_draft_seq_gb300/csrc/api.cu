@@ -54,7 +54,8 @@ size_t dspark_workspace_bytes(int32_t R, int32_t gamma, int32_t V, int32_t rank,
 
 dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
   if (!ws_ok(workspace, workspace_bytes, 256)) return DSPARK_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream));
+  // the whole workspace: the status word and every completion counter start at zero
+  return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
 }
 
 dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,

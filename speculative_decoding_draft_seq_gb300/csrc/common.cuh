@@ -29,29 +29,37 @@ struct WsLayout {
   size_t pend;     // int4   [R]             (kind, target row, prev token, accepted)
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
+  size_t vsplit;   // float4 [R][gamma+1][4] target row quarter stats (M_s, Z_s, max, argmax)
+  size_t vcount;   // u32    [R*(gamma+1) + R] row / request completion counters (zero between calls)
   size_t skey0, skey1, sidx0, sidx1;  // u32 [R*gamma] radix-sort ping-pong
   size_t fx;       // u64 [R*gamma]         fixed-point survivals / prefix sums in sorted order
   size_t fx2;      // u64 [R*gamma]         the same for the lagged confidences
   size_t total;
 };
 
+// Every section whose size does not depend on V comes first, so that the
+// scheduler (which lays the workspace out with V = 1) and the drafting and
+// verification calls (the real V) agree on all of them; the two V-sized
+// partial arrays come last.
 inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   WsLayout L;
   const size_t nc = (size_t)ceil_div(V, kChunk);
   const size_t n = (size_t)R * (size_t)gamma > 0 ? (size_t)R * (size_t)gamma : 1;
   size_t o = 0;
   L.status = o;  o = align256(o + 64 * sizeof(uint32_t));
-  L.dpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
+  L.vcount = o;  o = align256(o + ((size_t)R * (gamma + 1) + R) * sizeof(uint32_t));
   L.rowstat = o; o = align256(o + (size_t)R * (gamma + 1) * sizeof(float4));
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
-  L.rpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
   L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
+  L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * 4 * sizeof(float4));
   L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));
   L.skey1 = o;   o = align256(o + n * sizeof(uint32_t));
   L.sidx0 = o;   o = align256(o + n * sizeof(uint32_t));
   L.sidx1 = o;   o = align256(o + n * sizeof(uint32_t));
   L.fx = o;      o = align256(o + n * sizeof(unsigned long long));
   L.fx2 = o;     o = align256(o + n * sizeof(unsigned long long));
+  L.dpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
+  L.rpart = o;   o = align256(o + (size_t)R * nc * sizeof(float2));
   L.total = o;
   return L;
 }

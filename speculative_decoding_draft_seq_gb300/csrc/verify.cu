@@ -17,6 +17,8 @@
 //                  rejected position) or bonus weights P, chunk sums.
 //   resid_locate   one CTA per request: float64 scan of chunk sums, inverse
 //                  CDF, recompute of the crossing chunk, emitted token.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,7 +26,6 @@ namespace dspark {
 
 cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& launches, bool& taken);
 
-constexpr int kStatThreads = 512;
 constexpr int kRRows = 32;
 constexpr int kRKBlock = 32;
 
@@ -71,92 +72,216 @@ struct OnlineStat {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Target row statistics and the acceptance chain in one launch (rows a6, a7).
+//
+// Grid (R, gamma + 1, kVsSplit): CTA (r, k, s) streams the s-th quarter of
+// target row k of request r (rows past L_r return at once) and writes its
+// partial (max M_s, fixed-point sum Z_s of 2^((t - M_s) log2e/T) over its
+// threads, argmax) to the workspace. The last CTA of a row (a per-row counter,
+// reset by that CTA) combines the quarters: M = max M_s, Z = sum of the
+// quarters' sums rescaled to M (each term rounded once in float32, summed as
+// 2^-40 integers), the lowest-index argmax, and p(x_{k+1}). The last row of a
+// request to be combined (a per-request counter) runs the request's chain: one
+// warp tests the scheduled positions at once (u < p/q in float64), a ballot
+// finds the first rejection, and the accepted tokens, the pending residual or
+// bonus draw, and the zeroed p of unscheduled positions are written.
+constexpr int kVsThreads = 256;
+constexpr int kVsSplit = 4;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Streaming row statistics of 8 consecutive bf16 values (one 16-byte load):
+// sampled mode keeps (max m, sum of 2^(t kT - m kT)) with a running rescale,
+// greedy mode keeps (max, lowest index of the max).
+struct RowStat {
+  float m = -INFINITY, s = 0.f;
+  int ai = 0x7fffffff;
+  __device__ __forceinline__ void add8_sampled(const uint4& q, float kT) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    float t[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      t[2 * e] = __uint_as_float(w[e] << 16);
+      t[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+    const float gm = fmaxf(max3(t[0], t[1], t[2]), max3(t[3], t[4], max3(t[5], t[6], t[7])));
+    if (gm > m) {
+      s = m == -INFINITY ? 0.f : __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, gm), kT)));
+      m = gm;
+    }
+    const float mk = __fmul_rn(m, kT);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      a0 += ex2_approx(__fmaf_rn(t[i], kT, -mk));
+      a1 += ex2_approx(__fmaf_rn(t[i + 1], kT, -mk));
+    }
+    s += a0 + a1;
+  }
+  __device__ __forceinline__ void add8_greedy(const uint4& q, int v0) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    float t[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      t[2 * e] = __uint_as_float(w[e] << 16);
+      t[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+    const float gm = fmaxf(max3(t[0], t[1], t[2]), max3(t[3], t[4], max3(t[5], t[6], t[7])));
+    if (gm > m) {  // strict: the first index of a tie across groups stays
+      m = gm;
+      int i = 7;
+#pragma unroll
+      for (int j = 6; j >= 0; --j) i = t[j] == gm ? j : i;
+      ai = v0 + i;
+    }
+  }
+};
+
+// One work item: quarter sp of target row k (<= L) of request r.
 template <class Tin>
-__global__ void __launch_bounds__(kStatThreads) verify_stats_kernel(
+__device__ __forceinline__ void verify_row_item(
     int R, int gamma, int V, const Tin* __restrict__ target, const int32_t* __restrict__ tokens,
-    const int32_t* __restrict__ sched_len, float kT, int greedy, float4* __restrict__ rowstat,
-    float* __restrict__ p_tok, uint32_t* status) {
-  __shared__ float shf[32];
-  __shared__ int shi[32];
-  __shared__ unsigned long long shu[32];
-  const int r = blockIdx.x, k = blockIdx.y, tid = threadIdx.x;
-  const int L = min(max(sched_len[r], 0), gamma);
-  if (k > L) return;
-  const size_t row = ((size_t)r * (gamma + 1) + k) * V;
-  OnlineStat st;
-  // per-thread spans are interleaved in 8-element groups (coalesced 16-byte loads)
-  if (sizeof(Tin) == 2 && (V & 7) == 0) {
-    // four 16-byte loads in flight per thread per iteration (HBM latency)
+    const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, float kT, int greedy, uint64_t seed,
+    float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt, float4* rowstat, float* p_tok,
+    int32_t* __restrict__ out, int32_t* __restrict__ acc_len, int4* __restrict__ pend, uint32_t* status, int r,
+    int k, int sp, int L, float* shf, int* shi, unsigned long long* shu, volatile int& sLast) {
+  const int tid = threadIdx.x;
+  const size_t rowi = (size_t)r * (gamma + 1) + k;
+  const size_t row = rowi * V;
+  float am, Ms = 0.f, Zs = 0.f;
+  int ai;
+  if (sizeof(Tin) == 2 && (V & 7) == 0) {  // 8-element groups, eight 16-byte loads in flight per thread
+    RowStat st;
     const uint4* p = reinterpret_cast<const uint4*>(target + row);
     const int ng = V >> 3, T = blockDim.x;
-    for (int g0 = tid; g0 < ng; g0 += 4 * T) {
-      uint4 q[4];
+    const int gb = (int)(((long long)sp * ng) / kVsSplit), ge = (int)(((long long)(sp + 1) * ng) / kVsSplit);
+    for (int g0 = gb + tid; g0 < ge; g0 += 8 * T) {
+      uint4 q[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) q[u] = (g0 + u * T < ng) ? __ldg(p + g0 + u * T) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 8; ++u) q[u] = (g0 + u * T < ge) ? __ldcs(p + g0 + u * T) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (g0 + u * T >= ng) continue;
-        float t[8];
-        t[0] = bf16_bits_to_float(q[u].x & 0xffffu); t[1] = bf16_bits_to_float(q[u].x >> 16);
-        t[2] = bf16_bits_to_float(q[u].y & 0xffffu); t[3] = bf16_bits_to_float(q[u].y >> 16);
-        t[4] = bf16_bits_to_float(q[u].z & 0xffffu); t[5] = bf16_bits_to_float(q[u].z >> 16);
-        t[6] = bf16_bits_to_float(q[u].w & 0xffffu); t[7] = bf16_bits_to_float(q[u].w >> 16);
-        st.add8(t, (g0 + u * T) * 8, kT, greedy);
+      for (int u = 0; u < 8; ++u) {
+        if (g0 + u * T >= ge) continue;
+        if (greedy) st.add8_greedy(q[u], (g0 + u * T) * 8);
+        else st.add8_sampled(q[u], kT);
       }
     }
-  } else {
-    for (int v = tid; v < V; v += blockDim.x) st.add1(ld_elem(target, row + v), v, kT, greedy);
-  }
-  float am = st.am;
-  int ai = st.ai;
-  block_argmax(am, ai, shf, shi);
-  float M = 0.f, Zf = 1.f;
-  if (!greedy) {
-    // Z = sum over threads of s_t * 2^((m_t - M) log2e/T), each term rounded
-    // once in float32 and summed exactly as 2^-40 fixed-point integers
-    M = block_max(st.m, shf);
-    const float contrib = st.s > 0.f ? __fmul_rn(st.s, target_weight(st.m, M, kT)) : 0.f;
-    unsigned long long v = fx40(contrib);
+    am = st.m;
+    ai = st.ai;
+    if (greedy) {
+      block_argmax(am, ai, shf, shi);
+    } else {
+      Ms = block_max(st.m, shf);
+      const float contrib = st.s > 0.f ? __fmul_rn(st.s, ex2_approx(__fmul_rn(__fsub_rn(st.m, Ms), kT))) : 0.f;
+      unsigned long long v = fx40(contrib);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((tid & 31) == 0) shu[tid >> 5] = v;
-    __syncthreads();
-    unsigned long long Z = 0ull;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) Z += shu[i];
-    Zf = __fmul_rn((float)Z, 0x1p-40f);
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      __syncthreads();
+      if ((tid & 31) == 0) shu[tid >> 5] = v;
+      __syncthreads();
+      unsigned long long Z = 0ull;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) Z += shu[i];
+      Zs = __fmul_rn((float)Z, 0x1p-40f);
+      am = Ms;
+      ai = 0;
+    }
+  } else {  // any dtype or width: one element at a time
+    OnlineStat st;
+    const int vb = (int)(((long long)sp * V) / kVsSplit), ve = (int)(((long long)(sp + 1) * V) / kVsSplit);
+    for (int v = vb + tid; v < ve; v += blockDim.x) st.add1(ld_elem(target, row + v), v, kT, greedy);
+    am = st.am;
+    ai = st.ai;
+    block_argmax(am, ai, shf, shi);
+    if (!greedy) {
+      Ms = block_max(st.m, shf);
+      const float contrib = st.s > 0.f ? __fmul_rn(st.s, target_weight(st.m, Ms, kT)) : 0.f;
+      unsigned long long v = fx40(contrib);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      __syncthreads();
+      if ((tid & 31) == 0) shu[tid >> 5] = v;
+      __syncthreads();
+      unsigned long long Z = 0ull;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) Z += shu[i];
+      Zs = __fmul_rn((float)Z, 0x1p-40f);
+    }
   }
   if (tid == 0) {
-    rowstat[(size_t)r * (gamma + 1) + k] = make_float4(M, Zf, __int_as_float(ai), 0.f);
+    __stcg(vsplit + rowi * kVsSplit + sp, make_float4(Ms, Zs, am, __int_as_float(ai)));
+    __threadfence();
+    sLast = atomicAdd(row_cnt + rowi, 1u) == (unsigned)(kVsSplit - 1);
+  }
+  __syncthreads();
+  if (!sLast) return;
+
+  if (tid == 0) {  // combine the row's quarters
+    __threadfence();
+    row_cnt[rowi] = 0u;
+    float4 q[kVsSplit];
+#pragma unroll
+    for (int i = 0; i < kVsSplit; ++i) q[i] = __ldcg(vsplit + rowi * kVsSplit + i);
+    float bv = q[0].z, M = q[0].x;
+    int bi = __float_as_int(q[0].w);
+#pragma unroll
+    for (int i = 1; i < kVsSplit; ++i) {
+      const int ii = __float_as_int(q[i].w);
+      if (q[i].z > bv || (q[i].z == bv && ii < bi)) { bv = q[i].z; bi = ii; }
+      M = fmaxf(M, q[i].x);
+    }
+    // the weight formula of the streaming pass that produced the quarters
+    const bool fast = sizeof(Tin) == 2 && (V & 7) == 0;
+    auto wgt = [&](float t, float m) {
+      return fast ? ex2_approx(__fmaf_rn(t, kT, -__fmul_rn(m, kT))) : target_weight(t, m, kT);
+    };
+    float Zf = 1.f;
+    if (!greedy) {
+      unsigned long long Z = 0ull;
+#pragma unroll
+      for (int i = 0; i < kVsSplit; ++i)
+        if (q[i].y > 0.f) Z += fx40(__fmul_rn(q[i].y, fast ? ex2_approx(__fmul_rn(__fsub_rn(q[i].x, M), kT))
+                                                              : target_weight(q[i].x, M, kT)));
+      Zf = __fmul_rn((float)Z, 0x1p-40f);
+    } else {
+      M = 0.f;
+    }
+    __stcg(rowstat + rowi, make_float4(M, Zf, __int_as_float(bi), 0.f));
     if (k < L) {
       int x = tokens[(size_t)r * gamma + k];
       if (x < 0 || x >= V) { set_status(status, DSPARK_ERR_RANGE); x = min(max(x, 0), V - 1); }
-      float p;
-      if (greedy) p = (x == ai) ? 1.f : 0.f;
-      else p = __fdiv_rn(target_weight(ld_elem(target, row + x), M, kT), Zf);
-      p_tok[(size_t)r * gamma + k] = p;
+      float pv;
+      if (greedy) pv = (x == bi) ? 1.f : 0.f;
+      else pv = __fdiv_rn(wgt(ld_elem(target, row + x), M), Zf);
+      __stcg(p_tok + (size_t)r * gamma + k, pv);
     }
+    __threadfence();
+    sLast = atomicAdd(req_cnt + r, 1u) == (unsigned)L;  // rows 0..L of this request are combined
   }
-}
+  __syncthreads();
+  if (!sLast || tid >= 32) return;
 
-__global__ void __launch_bounds__(256) verify_chain_kernel(
-    int R, int gamma, const int32_t* __restrict__ tokens, const int32_t* __restrict__ anchor,
-    const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len, uint64_t seed, int greedy,
-    const float4* __restrict__ rowstat, float* __restrict__ p_tok, int32_t* __restrict__ out,
-    int32_t* __restrict__ acc_len, int4* __restrict__ pend) {
-  // one warp per request; lane l tests positions k = l + 1, l + 33, ... at once
-  const int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
-  if (r >= R) return;  // whole warps
-  const int L = min(max(sched_len[r], 0), gamma);
+  // the request's chain (warp 0)
+  const int lane = tid;
+  __threadfence();
+  if (lane == 0) req_cnt[r] = 0u;
   int A = L;
   for (int k0 = 1; k0 <= L; k0 += 32) {
-    const int k = k0 + lane;
+    const int kk = k0 + lane;
     bool fail = false;
-    if (k <= L) {
-      const float p = p_tok[(size_t)r * gamma + k - 1];
-      const float q = q_tok[(size_t)r * gamma + k - 1];
-      const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)k, kAccept);
-      fail = !((q <= 0.f) || (u < (double)p / (double)q));
+    if (kk <= L) {
+      const float pv = __ldcg(p_tok + (size_t)r * gamma + kk - 1);
+      const float qv = q_tok[(size_t)r * gamma + kk - 1];
+      const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)kk, kAccept);
+      fail = !((qv <= 0.f) || (u < (double)pv / (double)qv));
     }
     const unsigned m = __ballot_sync(0xffffffffu, fail);
     if (m) {  // the first rejected position k0 + ffs - 1 keeps A = k - 1 tokens
@@ -164,21 +289,42 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(
       break;
     }
   }
-  for (int k = lane; k <= gamma; k += 32) {
-    if (k < A) out[(size_t)r * (gamma + 1) + k] = tokens[(size_t)r * gamma + k];
-    else if (k > A) out[(size_t)r * (gamma + 1) + k] = -1;
-    if (k >= L && k < gamma) p_tok[(size_t)r * gamma + k] = 0.f;
+  for (int kk = lane; kk <= gamma; kk += 32) {
+    if (kk < A) out[(size_t)r * (gamma + 1) + kk] = tokens[(size_t)r * gamma + kk];
+    else if (kk > A) out[(size_t)r * (gamma + 1) + kk] = -1;
+    if (kk >= L && kk < gamma) p_tok[(size_t)r * gamma + kk] = 0.f;
   }
   if (lane == 0) {
     acc_len[r] = A;
     const int prev = A ? tokens[(size_t)r * gamma + A - 1] : anchor[r];
     if (greedy) {
-      out[(size_t)r * (gamma + 1) + A] = __float_as_int(rowstat[(size_t)r * (gamma + 1) + A].z);
+      out[(size_t)r * (gamma + 1) + A] = __float_as_int(__ldcg(rowstat + (size_t)r * (gamma + 1) + A).z);
       pend[r] = make_int4(kPendNone, A, prev, A);
     } else {
       pend[r] = make_int4(A < L ? kPendResid : kPendBonus, A, prev, A);
     }
   }
+}
+
+// One CTA per item. Grid (kVsSplit, R, gamma + 1): the quarters of a row are
+// launched together (the row combines sooner) and the small k, which are the
+// scheduled rows, first.
+template <class Tin>
+__global__ void __launch_bounds__(kVsThreads) verify_rows_kernel(
+    int R, int gamma, int V, const Tin* __restrict__ target, const int32_t* __restrict__ tokens,
+    const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len,
+    float kT, int greedy, uint64_t seed, float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt,
+    float4* rowstat, float* p_tok, int32_t* __restrict__ out, int32_t* __restrict__ acc_len,
+    int4* __restrict__ pend, uint32_t* status) {
+  __shared__ float shf[32];
+  __shared__ int shi[32];
+  __shared__ unsigned long long shu[32];
+  __shared__ int sLast;
+  const int sp = blockIdx.x, r = blockIdx.y, k = blockIdx.z;
+  const int L = min(max(sched_len[r], 0), gamma);
+  if (k > L) return;
+  verify_row_item<Tin>(R, gamma, V, target, tokens, anchor, q_tok, kT, greedy, seed, vsplit, row_cnt, req_cnt,
+                       rowstat, p_tok, out, acc_len, pend, status, r, k, sp, L, shf, shi, shu, sLast);
 }
 
 // Residual (or bonus) weight of one entry, with explicit rounding so the
@@ -367,12 +513,11 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
   const Tin* base = static_cast<const Tin*>(a.base);
   const Tin* W1 = static_cast<const Tin*>(a.W1);
   const Tin* W2 = static_cast<const Tin*>(a.W2);
-  verify_stats_kernel<Tin><<<dim3(a.R, a.gamma + 1), kStatThreads, 0, s>>>(
-      a.R, a.gamma, a.V, target, a.tokens, a.sched_len, kT, greedy, rowstat, a.p_tok, status);
-  verify_chain_kernel<<<ceil_div(a.R, 8), 256, 0, s>>>(a.R, a.gamma, a.tokens, a.anchor, a.q_tok,
-                                                          a.sched_len, a.seed, greedy, rowstat, a.p_tok,
-                                                          a.out_tokens, a.accepted_len, pend);
-  launches += 2;
+  verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma + 1), kVsThreads, 0, s>>>(
+      a.R, a.gamma, a.V, target, a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy, a.seed,
+      ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount), ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
+      rowstat, a.p_tok, a.out_tokens, a.accepted_len, pend, status);
+  launches += 1;
   if (!greedy) {
     bool taken = false;
     cudaError_t e = launch_resid_persistent(a, s, launches, taken);

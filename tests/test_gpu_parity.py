@@ -166,6 +166,31 @@ def test_deterministic_bits():
         assert np.array_equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("cfg", [RAGGED_FP32, W.with_(RAGGED_BF16, mode=W.LAGGED, conf_law="beta_mixed"),
+                                 TC_SHAPE], ids=["ragged_fp32", "ragged_bf16_lagged", "tc_shape"])
+def test_workspace_reused_across_rounds(cfg):
+    """Three rounds on one workspace (the scheduler and the verifier share it
+    with the drafting sweep): each equals a round on a fresh workspace, and the
+    first equals the oracle."""
+    inp = device_inputs(cfg)
+    R, gamma, V = inp["base"].shape
+    dt = dspark.BF16 if inp["base"].dtype == torch.bfloat16 else dspark.FP32
+    ws = dspark.new_workspace(R, gamma, V, inp["W1"].shape[1], dt, inp["sps"].numel())
+    fresh = gpu_round(cfg, inp)
+    o = oracle_round(cfg, list(range(cfg.R)))
+    for it in range(3):
+        out = dspark.RoundOutputs(R, gamma)
+        dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                      inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+        assert dspark.device_status(ws) == dspark.OK
+        got = out.host()
+        for k in ("tokens", "q_tok", "sched_len", "out_tokens", "accepted_len", "p_tok", "tau_theta"):
+            assert np.array_equal(got[k], fresh[k]), (it, k)
+        if it == 0:
+            got["status"] = dspark.OK
+            compare(cfg, got, o, list(range(cfg.R)))
+
+
 def test_device_generator_matches_numpy():
     cfg = W.CONFIGS["ds"]
     base, target = W.logits_device(W.with_(cfg, R=3), "cuda")
