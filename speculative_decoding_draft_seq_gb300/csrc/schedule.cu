@@ -314,24 +314,33 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 // Small problems (R * gamma <= kRankMaxKeys): one launch of many CTAs instead
 // of one CTA.
 //
-// Every CTA forms all the survival keys in shared memory; the rank of
-// candidate i in the ascending key order (ties by flat index) is the number
-// of candidates before it, counted by kRankSplit threads over interleaved
-// slices of the keys. The rank is the candidate's position in the order the
-// radix sort gives, so sfx[rank] = fixed_point(a) lays the survivals out in
-// sorted order. The last CTA to finish (a counter in the status block, reset
-// by that CTA) runs the admission: fixed-point inclusive scan of the sorted
-// survivals, the Theta comparisons as in schedule_kernel, and
-// L_r = #{j : rank(r, j) < K} (the order is prefix-closed within a request).
+// Every CTA forms all the survival keys and their fixed-point values in
+// shared memory. For each of its own kRankKeysPerCta candidates, kRankSplit
+// threads count over interleaved slices of the keys both the candidates
+// before it in the ascending key order (ties by flat index: the radix sort's
+// order) and the fixed-point sum of their survivals. So the CTA knows the
+// candidate's sorted position p and the exact prefix sums S_p (before it) and
+// S_p + f (with it), and evaluates the admission rule at that position:
+//   CAUSAL: admitting position p stops the scheduler iff B = R + p + 1 >
+//     n_table or Theta(S_p + f, SPS[B - 1]) < Theta(S_p, SPS[B - 2]); the
+//     smallest stopping position is K, gathered by an atomic max of n - p;
+//   LAGGED: Theta_{p+1} on the lagged order, written for the argmax;
+//   ALL: the survivals' sum, gathered by an atomic add.
+// The last CTA to finish (a counter in the status block; it resets every
+// counter it used) reads K (LAGGED: the smallest argmax of the Theta_i),
+// the prefix at K of the current order, and counts L_r = #{j : p(r, j) < K}
+// (the order is prefix-closed within a request).
 constexpr int kRankThreads = 256;
 constexpr int kRankSplit = 16;
 constexpr int kRankKeysPerCta = kRankThreads / kRankSplit;
 constexpr int kRankMaxKeys = 4096;
-constexpr size_t kSmallSmem = 2 * kRankMaxKeys * sizeof(uint32_t) + (kRankMaxKeys + 1) * sizeof(float);
+// keys + fixed-point survivals, current and lagged
+constexpr size_t kSmallSmem = 2 * (size_t)kRankMaxKeys * (sizeof(uint32_t) + sizeof(unsigned long long));
 
 // The confidences are staged in `key` by one coalesced pass, then each row's
-// running product overwrites them in place.
-__device__ void survival_keys_smem(const float* conf, int R, int gamma, uint32_t* key, uint32_t* status) {
+// running product overwrites them in place; fxv receives fixed_point(a).
+__device__ void survival_keys_smem(const float* conf, int R, int gamma, uint32_t* key, unsigned long long* fxv,
+                                   uint32_t* status) {
   const int n = R * gamma;
   stage_smem(key, reinterpret_cast<const uint32_t*>(conf), n);
   __syncthreads();
@@ -346,100 +355,92 @@ __device__ void survival_keys_smem(const float* conf, int R, int gamma, uint32_t
       c = c > 0.f ? fminf(c, 1.f) : 0.f;
       acc = __fmul_rn(acc, c);
       key[r * gamma + j] = survival_key(acc);
+      fxv[r * gamma + j] = fixed_point(acc);
     }
   }
 }
 
-// Rank of key i among key[0..n) (ties: smaller index first); every thread of
-// the group of kRankSplit lanes that holds i gets it.
-__device__ __forceinline__ int rank_of(const uint32_t* key, int n, int i, int s) {
+// Sorted position of candidate i and the fixed-point sum of the survivals
+// before it; every thread of the kRankSplit-lane group that holds i gets both.
+__device__ __forceinline__ void rank_and_prefix(const uint32_t* key, const unsigned long long* fxv, int n, int i,
+                                                int s, int& pos, unsigned long long& before_sum) {
   const uint32_t ki = key[min(i, n - 1)];
-  int before = 0;
-#pragma unroll 8
+  int cnt = 0;
+  unsigned long long sum = 0ull;
+#pragma unroll 4
   for (int j = s; j < n; j += kRankSplit) {
     const uint32_t kj = key[j];
-    before += (kj < ki) || (kj == ki && j < i);
+    const bool before = (kj < ki) || (kj == ki && j < i);
+    cnt += before;
+    sum += before ? fxv[j] : 0ull;
   }
 #pragma unroll
-  for (int o = kRankSplit / 2; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-  return before;
+  for (int o = kRankSplit / 2; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  }
+  pos = cnt;
+  before_sum = sum;
 }
 
-// In-place inclusive scan of v[0..n) in shared memory.
-__device__ void smem_inclusive_scan(unsigned long long* v, int n, unsigned long long* shu) {
-  const int T = blockDim.x, tid = threadIdx.x;
-  const int seg = ceil_div(n, T);
-  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-  unsigned long long loc = 0;
-  for (int i = s0; i < s1; ++i) loc += v[i];
-  unsigned long long tot;
-  unsigned long long run = block_exscan_u64(loc, shu, tot);
-  for (int i = s0; i < s1; ++i) {
-    run += v[i];
-    v[i] = run;
-  }
-  __syncthreads();
-}
-
-// Smallest argmax over the block of (value, index) pairs (float64 values).
-__device__ int block_argmax_d(double best, int besti, double* shd, int* shi) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-    if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
-  }
-  __syncthreads();
-  if (lane == 0) { shd[w] = best; shi[w] = besti; }
-  __syncthreads();
-  best = lane < nw ? shd[lane] : -INFINITY;
-  besti = lane < nw ? shi[lane] : 0x7fffffff;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-    if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
-  }
-  __syncthreads();
-  return besti;
+// float64 bits -> unsigned key with the same order
+__device__ __forceinline__ unsigned long long ordered_bits(double x) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
 __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
-    const float* __restrict__ sps, int n_table, int mode, uint32_t* rank_g, unsigned long long* sfx_g,
-    unsigned long long* sfx_lag_g, int32_t* __restrict__ L, int32_t* __restrict__ Kout,
-    double* __restrict__ tau_theta, unsigned int* done, uint32_t* status) {
-  // the two key arrays, reused by the last CTA as one u64 scan array, then the
-  // cost-table window SPS[R - 1 .. R + n - 1] (dynamic shared memory)
-  extern __shared__ __align__(16) uint32_t keys[];
-  float* swin = reinterpret_cast<float*>(keys + 2 * kRankMaxKeys);
-  __shared__ unsigned long long shu[32];
-  __shared__ int shi[32];
-  __shared__ double shd[32];
+    const float* __restrict__ sps, int n_table, int mode, uint32_t* pos_g, unsigned long long* prefix_g,
+    unsigned long long* theta_lag_g, int32_t* __restrict__ L, int32_t* __restrict__ Kout,
+    double* __restrict__ tau_theta, uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  unsigned long long* fxv = reinterpret_cast<unsigned long long*>(sm_raw);
+  unsigned long long* fxl = fxv + kRankMaxKeys;
+  uint32_t* key = reinterpret_cast<uint32_t*>(fxl + kRankMaxKeys);
+  uint32_t* keyl = key + kRankMaxKeys;
   __shared__ int sLast, sBad;
-  uint32_t* key = keys;
-  uint32_t* keyl = keys + kRankMaxKeys;
+  __shared__ unsigned long long sMax[kRankThreads / 32];
+  __shared__ int sMaxI[kRankThreads / 32];
+  unsigned int* done = status + 2;
+  unsigned long long* all_sum = reinterpret_cast<unsigned long long*>(status + 4);
+  unsigned int* stop_enc = status + 6;
   const int tid = threadIdx.x, T = blockDim.x;
   const int n = R * gamma;
   const bool lagged = mode == DSPARK_SCHED_LAGGED;
 
-  survival_keys_smem(conf, R, gamma, key, status);
-  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, status);
+  survival_keys_smem(conf, R, gamma, key, fxv, status);
+  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, fxl, status);
   __syncthreads();
   const int i = blockIdx.x * kRankKeysPerCta + tid / kRankSplit;
   const int s = tid % kRankSplit;
-  if (mode == DSPARK_SCHED_ALL) {  // no order needed: the sum is order-free
-    if (s == 0 && i < n) sfx_g[i] = fixed_point(key_survival(key[i]));
+  const bool mine = s == 0 && i < n;
+  const bool table_ok = R <= n_table;
+  if (mode == DSPARK_SCHED_ALL) {  // the sum is order-free: each CTA adds its own candidates
+    unsigned long long v = mine ? fxv[i] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((tid & 31) == 0 && v) atomicAdd(all_sum, v);
   } else {
-    const int rk = rank_of(key, n, i, s);
-    if (s == 0 && i < n) {
-      rank_g[i] = (uint32_t)rk;
-      sfx_g[rk] = fixed_point(key_survival(key[i]));
+    int p;
+    unsigned long long Sb;
+    rank_and_prefix(key, fxv, n, i, s, p, Sb);
+    if (mine) {
+      pos_g[i] = (uint32_t)p;
+      prefix_g[p] = Sb + fxv[i];  // inclusive prefix at sorted position p
+      if (mode == DSPARK_SCHED_CAUSAL && table_ok) {
+        const int B = R + p + 1;
+        bool st = B > n_table;
+        if (!st) st = theta_of(R, Sb + fxv[i], sps[B - 1]) < theta_of(R, Sb, sps[B - 2]);
+        if (st) atomicMax(stop_enc, (unsigned)(n - p));
+      }
     }
     if (lagged) {
-      const int rl = rank_of(keyl, n, i, s);
-      if (s == 0 && i < n) sfx_lag_g[rl] = fixed_point(key_survival(keyl[i]));
+      int pl;
+      unsigned long long Sl;
+      rank_and_prefix(keyl, fxl, n, i, s, pl, Sl);
+      if (mine && table_ok && pl + 1 <= min(n, n_table - R))  // Theta_{pl+1} of the lagged order
+        theta_lag_g[pl] = ordered_bits(theta_of(R, Sl + fxl[i], sps[R + pl]));
     }
   }
   __syncthreads();
@@ -450,9 +451,8 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   __syncthreads();
   if (!sLast) return;
   __threadfence();
-  if (tid == 0) *done = 0u;  // ready for the next call
 
-  unsigned long long* fx = reinterpret_cast<unsigned long long*>(keys);
+  // admission (last CTA)
   if (tid == 0) sBad = 0;
   __syncthreads();
   {
@@ -461,10 +461,15 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     for (int j = tid; j < n_table; j += T) bad |= !isfinite(__ldg(sps + j));
     if (bad) sBad = 1;
   }
-  // SPS entries R - 1 .. min(R + n, n_table) - 1, i.e. B = R .. R + n
-  const int w0 = max(R - 1, 0), w1 = min(R + n, n_table);
-  if (w1 > w0) stage_smem(swin, sps + w0, w1 - w0);
   __syncthreads();
+  const unsigned long long total = __ldcg(all_sum);
+  const unsigned int enc = __ldcg(stop_enc);
+  __syncthreads();
+  if (tid == 0) {  // every counter back to zero for the next call
+    *done = 0u;
+    *all_sum = 0ull;
+    *stop_enc = 0u;
+  }
   if (sBad) {
     if (tid == 0) {
       set_status(status, DSPARK_ERR_NONFINITE);
@@ -476,19 +481,15 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     return;
   }
   if (mode == DSPARK_SCHED_ALL) {
-    unsigned long long loc = 0;
-    for (int j = tid; j < n; j += T) loc += __ldcg(sfx_g + j);
-    unsigned long long tot;
-    block_exscan_u64(loc, shu, tot);
     for (int r = tid; r < R; r += T) L[r] = gamma;
     if (tid == 0) {
       *Kout = n;
-      tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(tot), 0x1p-40));
-      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, tot, sps[R + n - 1]) : 0.0;
+      tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(total), 0x1p-40));
+      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, total, sps[R + n - 1]) : 0.0;
     }
     return;
   }
-  if (R > n_table) {
+  if (!table_ok) {
     for (int r = tid; r < R; r += T) L[r] = 0;
     if (tid == 0) {
       *Kout = 0;
@@ -497,53 +498,40 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     }
     return;
   }
-
-  int K = 0;
-  if (lagged) {  // K = smallest argmax of Theta_i on the lagged order, i = 0..imax
-    stage_smem(fx, sfx_lag_g, n);
-    __syncthreads();
-    smem_inclusive_scan(fx, n, shu);
+  int K;
+  if (lagged) {  // smallest argmax of Theta_i, i = 0..imax (Theta_0 = Theta(R, 0))
     const int imax = min(n, n_table - R);
-    double best = -INFINITY;
+    unsigned long long best = 0ull;
     int besti = 0x7fffffff;
     for (int j = tid; j <= imax; j += T) {
-      const double th = theta_of(R, j ? fx[j - 1] : 0ull, swin[R + j - 1 - w0]);
+      const unsigned long long th =
+          j == 0 ? ordered_bits(theta_of(R, 0ull, sps[R - 1])) : __ldcg(theta_lag_g + (j - 1));
       if (th > best || (th == best && j < besti)) { best = th; besti = j; }
     }
-    K = block_argmax_d(best, besti, shd, shi);
-  }
-
-  stage_smem(fx, sfx_g, n);
-  __syncthreads();
-  smem_inclusive_scan(fx, n, shu);
-
-  if (mode == DSPARK_SCHED_CAUSAL) {  // the first admission that would lower Theta stops
-    int stop = 0x7fffffff;
-    for (int j = tid; j < n; j += T) {
-      const int B = R + j + 1;
-      bool st = B > n_table;
-      if (!st) {
-        const double th_next = theta_of(R, fx[j], swin[B - 1 - w0]);
-        const double th_prev = theta_of(R, j ? fx[j - 1] : 0ull, swin[B - 2 - w0]);
-        st = th_next < th_prev;
-      }
-      if (st) {
-        stop = j;
-        break;
-      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+      if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
     }
-    K = block_min_i(stop, shi);
-    if (K == 0x7fffffff) K = n;
+    if ((tid & 31) == 0) { sMax[tid >> 5] = best; sMaxI[tid >> 5] = besti; }
+    __syncthreads();
+    best = 0ull;
+    besti = 0x7fffffff;
+    for (int w = 0; w < T / 32; ++w)
+      if (sMax[w] > best || (sMax[w] == best && sMaxI[w] < besti)) { best = sMax[w]; besti = sMaxI[w]; }
+    K = besti;
+  } else {
+    K = enc ? n - (int)enc : n;
   }
   if (tid == 0) {
-    const unsigned long long S = K ? fx[K - 1] : 0ull;
+    const unsigned long long S = K ? __ldcg(prefix_g + (K - 1)) : 0ull;
     *Kout = K;
     tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
-    tau_theta[1] = theta_of(R, S, swin[R + K - 1 - w0]);
+    tau_theta[1] = theta_of(R, S, sps[R + K - 1]);
   }
-  uint32_t* srank = keys;  // the ranks, staged over the scan array
-  __syncthreads();
-  stage_smem(srank, rank_g, n);
+  uint32_t* srank = key;  // the positions, staged over the key array
+  stage_smem(srank, pos_g, n);
   __syncthreads();
   for (int r = tid; r < R; r += T) {
     int cnt = 0;
@@ -555,8 +543,9 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
 // Both scheduler forms behind one call: the many-CTA rank kernel (admission
 // in its last CTA) for small problems, the single-CTA radix sort otherwise.
 // Scratch: key0/key1/idx0/idx1 (u32[n] each), fx (u64[n]), for the small form
-// fx2 (u64[n]); status[0] is the sticky status word and status[2] the small
-// form's completion counter (zero between calls).
+// fx2 (u64[n]); status[0] is the sticky status word, status[2], [4..5] and
+// [6] the small form's completion counter, sum and stop word (zero between
+// calls).
 cudaError_t schedule_launch(const ScheduleArgs& a, uint32_t* key0, uint32_t* key1, uint32_t* idx0, uint32_t* idx1,
                             unsigned long long* fx, unsigned long long* fx2, uint32_t* status, cudaStream_t s,
                             int& launches) {
@@ -568,9 +557,9 @@ cudaError_t schedule_launch(const ScheduleArgs& a, uint32_t* key0, uint32_t* key
       cudaError_t e = set_smem_limit_once((const void*)schedule_small_kernel, (int)kSmallSmem, attr);
       if (e != cudaSuccess) return e;
     }
-    schedule_small_kernel<<<grid, kRankThreads, kSmallSmem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table,
-                                                        a.mode, key0, fx, fx2, a.sched_len, a.K, a.tau_theta,
-                                                        status + 2, status);
+    schedule_small_kernel<<<grid, kRankThreads, kSmallSmem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps,
+                                                                 a.n_table, a.mode, key0, fx, fx2, a.sched_len, a.K,
+                                                                 a.tau_theta, status);
     launches += 1;
     return cudaGetLastError();
   }
