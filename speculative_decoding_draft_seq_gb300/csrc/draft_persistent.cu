@@ -817,8 +817,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* baseEmpty = baseFull + 2 * kPBaseStages;
   uint64_t* accFull = baseEmpty + 2 * kPBaseStages;
   uint64_t* accEmpty = accFull + 2;
-  uint64_t* aFull = accEmpty + 2;
-  uint64_t* drain = aFull + 1;
+  uint64_t* aFull = accEmpty + 2;  // [4]: one per 64-column K box of A
+  uint64_t* drain = aFull + 4;
   uint64_t* w1Full = drain + 1;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(w1Full + 1);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
@@ -835,7 +835,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int i = 0; i < kPBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
     for (int i = 0; i < 2 * kPBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kPEpiWarps); }
-    mbar_init(aFull, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&aFull[i], 1);
     mbar_init(drain, 1);
     mbar_init(w1Full, 1);
     *sAbort = 0;
@@ -903,9 +903,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bool stop = false;
       for (int k = 1; k <= n_steps && !stop; ++k)
         for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
-          if (!mbar_wait(aFull, a_use & 1, sAbort, p.status)) { stop = true; break; }
+          // the A boxes are awaited one by one, as the first tile reaches them
+          const uint32_t apar = (uint32_t)(a_use & 1);
           ++a_use;
-          tc_fence_after();
+          uint32_t a_ready = 0;
           for (int t = 0; t < n_tiles && !stop; ++t, ++T) {
             const int buf = T & 1;
             const uint32_t use = (uint32_t)(T >> 1);
@@ -916,6 +917,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t d = tmem + (uint32_t)(buf * 256);
             for (int kc = 0; kc < nkc; ++kc, ++n) {
               const int stage = n % kBStages;
+              const int ka = (kc * kPKC) >> 6;
+              if (!((a_ready >> ka) & 1u)) {
+                if (!mbar_wait(&aFull[ka], apar, sAbort, p.status)) { stop = true; break; }
+                a_ready |= 1u << ka;
+              }
               if (!mbar_wait(&bFull[stage], (n / kBStages) & 1, sAbort, p.status)) { stop = true; break; }
               tc_fence_after();
               // K rows [kc * kPKC, +kPKC): A chunk of 64 K-columns, then 32-byte K16 steps inside it
@@ -943,6 +949,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     int T = 0, nh = 0;
     unsigned int epoch = 0;
     uint32_t w1_use = 0;
+    uint32_t a_phases = 0;  // A-operand phases completed by this group (both gather paths)
     const uint64_t pol_a = l2_policy_evict_last();
     bool stop = false;
     for (int k = 1; k <= n_steps && !stop; ++k) {
@@ -955,9 +962,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (et == 0) {
             const int nka = p.rank / 64;
             fence_proxy_async_global();
-            mbar_expect_tx(aFull, (uint32_t)(nka * p.box_rows * 128));
-            for (int ka = 0; ka < nka; ++ka)
-              tma_load_3d(sA + ka * kPAChunk, &mapA, ka * 64, mt * kPM, (k - 1) & 1, aFull, pol_a);
+            for (int ka = 0; ka < 4; ++ka) {
+              if (ka < nka) {
+                mbar_expect_tx(&aFull[ka], (uint32_t)(p.box_rows * 128));
+                tma_load_3d(sA + ka * kPAChunk, &mapA, ka * 64, mt * kPM, (k - 1) & 1, &aFull[ka], pol_a);
+              } else {
+                mbar_arrive(&aFull[ka]);  // unused box: keeps the four phases in step
+              }
+            }
           }
         } else {  // two threads per row: one token load, then 16 independent 16-byte loads each
           const int m = et >> 1, j0 = (et & 1) * 16, r = mt * kPM + m;
@@ -986,8 +998,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           fence_proxy_async_smem();
           eg_sync();
-          if (et == 0) mbar_arrive(aFull);
+          if (et == 0)
+            for (int ka = 0; ka < 4; ++ka) mbar_arrive(&aFull[ka]);
         }
+        ++a_phases;
 
         ResidRow rr{};
         ResidCopyRows cr{};
@@ -1130,6 +1144,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
     if (kResid) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
+    if (et == 0 && a_phases > 0)  // nor an A box the MMA issuer stopped waiting for
+      for (int ka = 0; ka < 4; ++ka) mbar_wait_drain(&aFull[ka], (a_phases - 1) & 1, p.status);
     *sAbort = (*sAbort) | (stop ? 1 : 0);  // let the other roles wind down
     (void)ew;
   }
