@@ -956,30 +956,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int mt = 0; mt < p.n_mt && !stop; ++mt) {
         // A = W1[prev] rows of this M tile (the previous MMAs on sA are done:
         // every tile of the previous tile sequence was received below)
-        if (!kResid && k > 1) {
-          // the rows staged by the CTAs that drew the tokens of step k - 1
-          // (visible since the grid barrier): four TMA boxes of 64 K-columns
+        if (kResid || k > 1) {
+          // drafting: the rows staged by the CTAs that drew the tokens of step
+          // k - 1 (visible since the grid barrier); residual pass: the rows the
+          // verifier's chain staged (previous launch). Four TMA boxes of 64
+          // K-columns.
           if (et == 0) {
             const int nka = p.rank / 64;
             fence_proxy_async_global();
             for (int ka = 0; ka < 4; ++ka) {
               if (ka < nka) {
                 mbar_expect_tx(&aFull[ka], (uint32_t)(p.box_rows * 128));
-                tma_load_3d(sA + ka * kPAChunk, &mapA, ka * 64, mt * kPM, (k - 1) & 1, &aFull[ka], pol_a);
+                tma_load_3d(sA + ka * kPAChunk, &mapA, ka * 64, mt * kPM, kResid ? 0 : (k - 1) & 1, &aFull[ka],
+                            pol_a);
               } else {
                 mbar_arrive(&aFull[ka]);  // unused box: keeps the four phases in step
               }
             }
           }
-        } else {  // two threads per row: one token load, then 16 independent 16-byte loads each
+        } else {  // k == 1: the anchors' rows, two threads per row, 16 independent 16-byte loads each
           const int m = et >> 1, j0 = (et & 1) * 16, r = mt * kPM + m;
           int prev = -1;
-          if (kResid) {
-            if (r < p.R) {
-              const int4 pd = __ldg(p.pend + r);
-              prev = (pd.x == kPendResid) ? min(max(pd.z, 0), p.V - 1) : -1;
-            }
-          } else if (r < p.R) {  // k == 1: the anchors
+          if (r < p.R) {
             prev = __ldg(p.anchor + r);
             if (prev < 0 || prev >= p.V) {
               set_status(p.status, DSPARK_ERR_RANGE);
@@ -1266,6 +1264,13 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
     if (!make_tmap_bf16(&mapW2, a.W2, 2, dims, strides, box)) return cudaSuccess;
   }
   const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  CUtensorMap mapA;  // the A rows the verifier staged in astage[0]
+  {
+    const uint64_t dims[3] = {(uint64_t)a.rank, (uint64_t)a.R, 2};
+    const uint64_t strides[2] = {(uint64_t)a.rank * 2, (uint64_t)a.R * a.rank * 2};
+    const uint32_t box[3] = {64, (uint32_t)(a.R < kPM ? a.R : kPM), 1};
+    if (!make_tmap_bf16(&mapA, ws_at<void>(a.ws, L.astage), 3, dims, strides, box)) return cudaSuccess;
+  }
   PersistParams p{};
   p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
   p.nc = ceil_div(a.V, kChunk);
@@ -1290,7 +1295,7 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapW2, &mapW2, &p};  // no base or staged-row map in residual mode
+  void* args[] = {&mapW2, &mapW2, &mapA, &p};  // no base map in residual mode
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;

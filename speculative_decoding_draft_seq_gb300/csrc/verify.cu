@@ -153,8 +153,9 @@ __device__ __forceinline__ void verify_row_item(
     int R, int gamma, int V, const Tin* __restrict__ target, const int32_t* __restrict__ tokens,
     const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, float kT, int greedy, uint64_t seed,
     float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt, float4* rowstat, float* p_tok,
-    int32_t* __restrict__ out, int32_t* __restrict__ acc_len, int4* __restrict__ pend, uint32_t* status, int r,
-    int k, int sp, int L, float* shf, int* shi, unsigned long long* shu, volatile int& sLast) {
+    int32_t* __restrict__ out, int32_t* __restrict__ acc_len, int4* __restrict__ pend, uint32_t* status,
+    const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage, int r, int k, int sp, int L, float* shf, int* shi,
+    unsigned long long* shu, volatile int& sLast) {
   const int tid = threadIdx.x;
   const size_t rowi = (size_t)r * (gamma + 1) + k;
   const size_t row = rowi * V;
@@ -304,6 +305,17 @@ __device__ __forceinline__ void verify_row_item(
       pend[r] = make_int4(A < L ? kPendResid : kPendBonus, A, prev, A);
     }
   }
+  // The residual pass's A row of this request (rank > 0 only when the
+  // tensor-core residual pass can run: bf16, rank a multiple of 64 up to 256,
+  // W1 16-byte aligned): W1[prev] for a residual draw, zeros otherwise
+  // (finite, so the MMA row is finite).
+  if (rank > 0 && !greedy && 8 * lane < rank) {
+    const int prev = min(max(A ? tokens[(size_t)r * gamma + A - 1] : anchor[r], 0), V - 1);
+    const uint4 w = A < L ? __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)prev * rank) + lane)
+                          : make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(astage + (size_t)r * rank)[lane] = w;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
 }
 
 // One CTA per item. Grid (kVsSplit, R, gamma + 1): the quarters of a row are
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kVsThreads) verify_rows_kernel(
     const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len,
     float kT, int greedy, uint64_t seed, float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt,
     float4* rowstat, float* p_tok, int32_t* __restrict__ out, int32_t* __restrict__ acc_len,
-    int4* __restrict__ pend, uint32_t* status) {
+    int4* __restrict__ pend, uint32_t* status, const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage) {
   __shared__ float shf[32];
   __shared__ int shi[32];
   __shared__ unsigned long long shu[32];
@@ -324,7 +336,8 @@ __global__ void __launch_bounds__(kVsThreads) verify_rows_kernel(
   const int L = min(max(sched_len[r], 0), gamma);
   if (k > L) return;
   verify_row_item<Tin>(R, gamma, V, target, tokens, anchor, q_tok, kT, greedy, seed, vsplit, row_cnt, req_cnt,
-                       rowstat, p_tok, out, acc_len, pend, status, r, k, sp, L, shf, shi, shu, sLast);
+                       rowstat, p_tok, out, acc_len, pend, status, W1, rank, astage, r, k, sp, L, shf, shi, shu,
+                       sLast);
 }
 
 // Residual (or bonus) weight of one entry, with explicit rounding so the
@@ -513,10 +526,13 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
   const Tin* base = static_cast<const Tin*>(a.base);
   const Tin* W1 = static_cast<const Tin*>(a.W1);
   const Tin* W2 = static_cast<const Tin*>(a.W2);
+  const int stage_rank = (sizeof(Tin) == 2 && a.rank % 64 == 0 && a.rank <= 256 &&
+                          (reinterpret_cast<uintptr_t>(a.W1) & 15) == 0) ? a.rank : 0;
   verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma + 1), kVsThreads, 0, s>>>(
       a.R, a.gamma, a.V, target, a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy, a.seed,
       ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount), ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
-      rowstat, a.p_tok, a.out_tokens, a.accepted_len, pend, status);
+      rowstat, a.p_tok, a.out_tokens, a.accepted_len, pend, status, W1, stage_rank,
+      ws_at<__nv_bfloat16>(ws, L.astage));
   launches += 1;
   if (!greedy) {
     bool taken = false;
