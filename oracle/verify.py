@@ -32,9 +32,12 @@ Pins (tests/test_oracle_verify.py): exact enumeration of the output law at
 V <= 4, gamma <= 3 over every draft sequence and accept/reject branch equals
 the target rows; chi-square of emitted tokens at V <= 16 over many requests;
 empirical position-1 acceptance equals sum_v min(P, Q); the worked round of
-the pages; an anticipating scheduler fails the same enumeration. Parity of
-the residual/bonus sampler at full vocabulary size is unpinned except through
-these small-V pins.
+the pages; an anticipating scheduler fails the same enumeration. At the full
+vocabulary (V = 129280, rank 256), closed forms: a target row equal to the
+drafter's logits with the drafted token pushed down and exactly its mass moved
+onto a second token makes the residual a point mass there (a draw from P or Q
+would not be); a boosted token is the residual's point mass; a dominant token
+is the bonus.
 """
 
 import numpy as np

@@ -150,3 +150,90 @@ def test_forced_rejection_draws_from_residual(monkeypatch):
     v = Vf.verify_request(target, base, 0, W1, W2, d["tokens"], 1, 1.0, seed=0, r=0)
     assert v["A"] == 0 and list(v["out"]) == [1]
     assert v["p"][0] == 0.0 and v["q"][0] == pytest.approx(0.5)
+
+
+def _full_vocab_case(seed, V=129280, rank=256, gamma=2):
+    rng = np.random.default_rng(seed)
+    base = rng.normal(0, 1.5, size=(gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.02, size=(V, rank))
+    W2 = rng.normal(0, 0.02, size=(rank, V))
+    return base, W1, W2
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_full_vocab_residual_is_the_boosted_token(T):
+    """Closed form at the full DeepSeek-scale vocabulary (V = 129280, rank 256):
+    if target row 0 equals the drafter's logits at position 1 except for one
+    token v* raised by D, then P(v) < Q(v) for every v != v* and P(v*) > Q(v*),
+    so normalize(max(0, P - Q)) is the point mass at v*; with D large, the
+    drafted token (not v*) is rejected, and the corrected token must be v*
+    whatever the uniform. Pins the residual construction and its sampler at
+    full size, where no enumeration is possible."""
+    V, gamma = 129280, 2
+    base, W1, W2 = _full_vocab_case(11, V=V, gamma=gamma)
+    anchor = 4242
+    l1 = base[0].astype(np.float64) + W1[anchor] @ W2
+    for vstar in (int(np.argmin(l1)), 77777):
+        target = np.stack([l1, base[1], base[1]]).astype(np.float32)
+        target[0, vstar] = np.float32(l1[vstar] + 60.0 * T)
+        for seed in (0, 1, 2):
+            d = D.draft_request(base, anchor, W1, W2, T, seed, 0)
+            assert d["tokens"][0] != vstar
+            v = Vf.verify_request(target, base, anchor, W1, W2, d["tokens"], 2, T, seed, 0)
+            assert v["A"] == 0
+            assert v["new_token"] == vstar
+
+
+def test_full_vocab_bonus_is_the_dominant_token():
+    """Closed form: when every scheduled token is accepted (target rows equal
+    the drafter's logits exactly, so p = q and u < 1 accepts), the bonus token
+    is drawn from the next target row; a row whose one logit exceeds the rest
+    by 80/T puts all but ~e^-80 of its mass there, so the bonus is that token."""
+    V, gamma, T = 129280, 2, 1.0
+    base, W1, W2 = _full_vocab_case(12, V=V, gamma=gamma)
+    anchor = 99
+    d = D.draft_request(base, anchor, W1, W2, T, 3, 0)
+    rows = []
+    prev = anchor
+    for k in range(gamma):
+        rows.append(base[k].astype(np.float64) + W1[prev] @ W2)
+        prev = int(d["tokens"][k])
+    bonus_row = base[1].astype(np.float64).copy()
+    vstar = 123456
+    bonus_row[vstar] = bonus_row.max() + 80.0
+    target = np.stack(rows + [bonus_row]).astype(np.float32)
+    v = Vf.verify_request(target, base, anchor, W1, W2, d["tokens"], gamma, T, 3, 0)
+    # p and q come from the same float32 logits up to the float32 rounding of
+    # the drafter's float64 logits, so every ratio is 1 to ~1e-6 and u < 1
+    assert v["A"] == gamma
+    assert v["new_token"] == vstar
+
+
+@pytest.mark.parametrize("T", [1.0, 0.8])
+def test_full_vocab_residual_moves_mass_of_rejected_token(T):
+    """Closed form at V = 129280 that tells the residual apart from P and Q:
+    target row 0 = the drafter's logits at position 1, with the drafted token
+    x1 pushed down by 60 T (its acceptance ratio is ~e^-60: rejected) and a
+    second token v1 raised by b = T ln(1 + e^((l_x1 - l_v1)/T)(1 - e^-60)),
+    which moves exactly x1's mass onto v1. Then P = Q off {x1, v1}, so
+    max(0, P - Q) is the point mass at v1 and the corrected token is v1 for
+    every uniform, while a draw from P or Q would give v1 only with
+    probability about Q(x1)."""
+    V = 129280
+    base, W1, W2 = _full_vocab_case(13, V=V)
+    anchor = 31337
+    l1 = base[0].astype(np.float64) + W1[anchor] @ W2
+    for seed in (0, 1, 2, 3):
+        d = D.draft_request(base, anchor, W1, W2, T, seed, 0)
+        x1 = int(d["tokens"][0])
+        v1 = int(np.argsort(l1)[V // 2])  # a token of middling probability, != x1
+        if v1 == x1:
+            v1 = int(np.argsort(l1)[V // 2 + 1])
+        b = T * np.log1p(np.exp((l1[x1] - l1[v1]) / T) * (1.0 - np.exp(-60.0)))
+        row0 = l1.copy()
+        row0[x1] -= 60.0 * T
+        row0[v1] += b
+        target = np.stack([row0, base[1], base[1]]).astype(np.float32)
+        v = Vf.verify_request(target, base, anchor, W1, W2, d["tokens"], 2, T, seed, 0)
+        assert v["A"] == 0
+        assert v["new_token"] == v1
