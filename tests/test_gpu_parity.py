@@ -166,6 +166,28 @@ def test_deterministic_bits():
         assert np.array_equal(a[k], b[k]), k
 
 
+TC_SWEEP = [
+    # (R, gamma, V, rank): the tensor-core drafting sweep and residual pass at other shapes
+    (200, 3, 2056, 128),   # 200 requests: two M tiles, CTAs drawing two requests per step
+    (1, 5, 1000, 64),      # a single request
+    (64, 1, 4104, 192),    # gamma = 1, rank 192, a vocabulary tail of 8 columns
+    (33, 6, 640, 256),     # fewer chunks than SMs: ten CTAs
+]
+
+
+@pytest.mark.parametrize("R,gamma,V,rank", TC_SWEEP)
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tensor_core_path_shapes(R, gamma, V, rank, T):
+    cfg = W.Workload(f"tc_{R}_{gamma}_{V}_{rank}", R=R, gamma=gamma, V=V, rank=rank, dtype="bf16", T=T,
+                     mode=W.CAUSAL, seed=4000 + R + gamma + rank, base_sd=1.5, w_sd=0.05, target_sd=(0.45,),
+                     conf_law="decreasing", table="concave", n_table=R * (gamma + 1))
+    rep, g, _ = _full(cfg)
+    assert rep["positions"] > 0
+    # one persistent drafting launch, the scheduler, the row stats, and (sampled) the residual
+    # sweep: the tensor-core path, not the per-step or CUDA-core fallbacks
+    assert g["launches"] == (4 if T > 0 else 3), g["launches"]
+
+
 @pytest.mark.parametrize("cfg", [RAGGED_FP32, W.with_(RAGGED_BF16, mode=W.LAGGED, conf_law="beta_mixed"),
                                  TC_SHAPE], ids=["ragged_fp32", "ragged_bf16_lagged", "tc_shape"])
 def test_workspace_reused_across_rounds(cfg):
