@@ -88,8 +88,9 @@ class ClockSampler:
         self.path = None
 
     def start(self, rank):
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+        out_dir = os.environ.get("DSPARK_OUT_DIR", os.path.join(ROOT, "runs"))
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_rank{rank}.csv")
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")

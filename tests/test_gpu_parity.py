@@ -79,8 +79,9 @@ def test_full_size_sampled(name, T, requests):
     o = oracle_round(cfg, requests)
     rep = compare(cfg, g, o, requests)
     rep = {k: (float(v) if isinstance(v, (float, np.floating)) else v) for k, v in rep.items()}
-    os.makedirs("gpurun_out", exist_ok=True)
-    with open(os.path.join("gpurun_out", "parity_reports.jsonl"), "a") as f:
+    out_dir = os.environ.get("DSPARK_OUT_DIR", "runs")
+    os.makedirs(out_dir, exist_ok=True)
+    with open(os.path.join(out_dir, "parity_reports.jsonl"), "a") as f:
         f.write(json.dumps({"workload": name, "T": T, "requests": requests, **rep}) + "\n")
 
 
