@@ -201,6 +201,35 @@ dspark_status dspark_verify(int32_t R, int32_t gamma, int32_t V, int32_t rank, i
                             size_t workspace_bytes, dspark_stream_t stream);
 
 /*
+ * Acceptance labels of the confidence head (GeekNews page, "Confidence head"
+ * and "Calibração posterior": the head predicts the probability that each
+ * drafted token passes verification). For every request r and position
+ * k = 1..gamma,
+ *   labels[r, k-1] = 1 - (1/2) sum_v |Q_k(v) - P_{k-1}(v)|  (one minus the
+ *                    total variation distance = sum_v min(P_{k-1}, Q_k)),
+ * Q_k the drafter's distribution at position k given the drafted tokens
+ * before it, P_{k-1} the target's row k-1, both at `temperature`; for
+ * temperature 0 both are one-hot and the label is 1 where the drafted token
+ * is the target row's argmax (lowest index on ties), else 0.
+ *
+ *   target_logits, base_logits, anchor, W1, W2   as for dspark_verify
+ *   draft_tokens [R, gamma] int32, q_stats [R, gamma, 2]  outputs of dspark_draft_sequential
+ *   labels       [R, gamma] float out
+ * Every position is labelled, whatever a scheduler would admit. Sampled mode
+ * (temperature > 0) needs the tensor-core shape: bf16 inputs, rank a multiple
+ * of 64 up to 256, V a multiple of 8 and at least 64, 16-byte aligned
+ * pointers, and cooperative launch; otherwise it returns
+ * DSPARK_ERR_INVALID_ARG and enqueues nothing it would need. Uses the same
+ * workspace as the other calls.
+ */
+dspark_status dspark_acceptance_labels(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                       const void* target_logits, const void* base_logits,
+                                       const int32_t* anchor, const void* W1, const void* W2,
+                                       const int32_t* draft_tokens, const float* q_stats, float temperature,
+                                       float* labels, void* workspace, size_t workspace_bytes,
+                                       dspark_stream_t stream);
+
+/*
  * One whole round: draft -> schedule -> verify on one stream, with no host
  * synchronisation in between (the scheduled lengths stay on the device).
  * Arguments are the union of the three calls above; the intermediate outputs

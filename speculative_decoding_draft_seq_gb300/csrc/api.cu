@@ -8,6 +8,7 @@
 #include "internal.h"
 
 namespace dspark {
+bool draft_tc_eligible(const DraftArgs& a);
 cudaError_t launch_draft_cuda_core(const DraftArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_draft_tc(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken);
 cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken);
@@ -151,6 +152,37 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
     e = launch_verify(va, s, n);
   }
   g_last_launches = n;
+  return cuda_status(e);
+}
+
+dspark_status dspark_acceptance_labels(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                       const void* target_logits, const void* base_logits,
+                                       const int32_t* anchor, const void* W1, const void* W2,
+                                       const int32_t* draft_tokens, const float* q_stats, float temperature,
+                                       float* labels, void* workspace, size_t workspace_bytes,
+                                       dspark_stream_t stream) {
+  g_last_launches = 0;
+  if (!dims_ok(R, gamma, V, rank, dtype) || !(temperature >= 0.f) || !isfinite(temperature))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!target_logits || !base_logits || !anchor || !W1 || !W2 || !draft_tokens || !q_stats || !labels)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!ws_ok(workspace, workspace_bytes, ws_layout(R, gamma, V).total)) return DSPARK_ERR_WORKSPACE;
+  if (temperature > 0.f) {  // decide support before enqueueing anything
+    DraftArgs d{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, temperature, 0,
+                nullptr, nullptr, nullptr, workspace};
+    int dev = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (!draft_tc_eligible(d) || (reinterpret_cast<uintptr_t>(target_logits) & 15) != 0 || !coop)
+      return DSPARK_ERR_INVALID_ARG;
+  }
+  LabelArgs a{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens, q_stats,
+              temperature, labels, workspace};
+  int n = 0;
+  bool supported = true;
+  cudaError_t e = launch_labels(a, (cudaStream_t)stream, n, supported);
+  g_last_launches = n;
+  if (e == cudaSuccess && !supported) return DSPARK_ERR_INVALID_ARG;
   return cuda_status(e);
 }
 

@@ -31,6 +31,8 @@ struct WsLayout {
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
   size_t vsplit;   // float4 [R][gamma+1][4] target row quarter stats (M_s, Z_s, max, argmax)
   size_t vcount;   // u32    [R*(gamma+1) + R] row / request completion counters (zero between calls)
+  size_t lstage;   // bf16   [R*gamma][256]  acceptance labels: W1 rows of every (request, position)
+  size_t lsum;     // u64    [R*gamma]       acceptance labels: 2^-40 sums of max(0, P - Q) (zero between calls)
   size_t skey0, skey1, sidx0, sidx1;  // u32 [R*gamma] radix-sort ping-pong
   size_t fx;       // u64 [R*gamma]         fixed-point survivals / prefix sums in sorted order
   size_t fx2;      // u64 [R*gamma]         the same for the lagged confidences
@@ -52,6 +54,8 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
   L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
   L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * 4 * sizeof(float4));
+  L.lstage = o;  o = align256(o + (size_t)R * gamma * 256 * 2);
+  L.lsum = o;    o = align256(o + (size_t)R * gamma * sizeof(unsigned long long));
   L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));
   L.skey1 = o;   o = align256(o + n * sizeof(uint32_t));
   L.sidx0 = o;   o = align256(o + n * sizeof(uint32_t));

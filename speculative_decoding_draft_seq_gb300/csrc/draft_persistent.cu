@@ -88,6 +88,10 @@ struct PersistParams {
   const float4* rowstat;        // target row stats (M, Z, argmax, -)
   int32_t* out_tokens;          // [R, gamma+1]
   float2* rpart;                // [R][nc] (sum max(0, P - Q), sum P)
+  // acceptance labels (one pass over every (request, position) pair)
+  int n_pairs;                  // R * gamma
+  unsigned long long* lsum;     // [R * gamma] 2^-40 sums of max(0, P - Q), zero between calls
+  float* labels;                // [R, gamma]
 };
 
 // Per-request constants of the residual pass: P(v) = 2^((t_v - M_P) log2e/T) / Z_P
@@ -526,6 +530,28 @@ __device__ __forceinline__ ResidRow load_resid_row(const PersistParams& p, int r
   return rr;
 }
 
+// Acceptance-label pass: row pr is the pair (request r = pr / gamma, position
+// k = pr % gamma + 1): Q from the drafting stats of position k, P from target
+// row k - 1; both rows of every pair are read (kind = residual).
+__device__ __forceinline__ ResidRow load_label_row(const PersistParams& p, int pr) {
+  ResidRow rr;
+  rr.kind = kPendNone;
+  rr.A = 0;
+  rr.MPk = rr.invZP = rr.MQk = rr.invZQ = 0.f;
+  if (pr < p.n_pairs) {
+    const int r = pr / p.gamma, k1 = pr - r * p.gamma;
+    rr.kind = kPendResid;
+    rr.A = k1;
+    const float4 rs = __ldg(p.rowstat + (size_t)r * (p.gamma + 1) + k1);
+    rr.MPk = __fmul_rn(rs.x, p.kT);
+    rr.invZP = __frcp_rn(rs.y);
+    const size_t qi = 2 * ((size_t)r * p.gamma + k1);
+    rr.MQk = __fmul_rn(__ldg(p.q_stats + qi), p.kT);
+    rr.invZQ = __frcp_rn(__ldg(p.q_stats + qi + 1));
+  }
+  return rr;
+}
+
 __device__ __forceinline__ float unpack_bf16(const uint4& x, int e) {
   const uint32_t w = e < 2 ? x.x : (e < 4 ? x.y : (e < 6 ? x.z : x.w));
   return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
@@ -798,7 +824,7 @@ namespace dspark {
 // kResid = false: the gamma drafting steps. kResid = true: one pass of the
 // verifier's residual / bonus draw (A rows = W1[prev] of each request's
 // first rejected position, per-request target and base rows read directly).
-template <bool kResid>
+template <bool kResid, bool kLabel = false>
 __global__ void __launch_bounds__(kPThreads, 1)
     persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                             const __grid_constant__ CUtensorMap mapA, PersistParams p) {
@@ -1012,10 +1038,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           return c < c_end ? c * 64 + 32 * (sidx & 1) : -1;
         };
         int hs = 0;
+        unsigned long long lacc = 0ull;  // label pass: this thread's 2^-40 sum over its chunks
+        const int pr = mt * kPM + row;   // the request (residual) or the (request, position) pair (labels)
         if (kResid) {
           __syncwarp();  // the previous M tile's reads of the buffers are done
-          rr = load_resid_row(p, mt * kPM + row);
-          cr = resid_copy_rows(p, rr, mt * kPM + row, lane);
+          rr = kLabel ? load_label_row(p, pr) : load_resid_row(p, pr);
+          cr = resid_copy_rows(p, rr, kLabel ? pr / p.gamma : pr, lane);
           resid_issue(p, cr, hc_col(0), lane, rs_base);
           resid_issue(p, cr, hc_col(1), lane, rs_base + kRsBufBytes);
         }
@@ -1039,9 +1067,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                            tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh),
                            sBase + (size_t)ew * kRsWarpBytes + (size_t)(hs % kRsBufs) * kRsBufBytes, lane, sw, sp);
               }
-              if (rr.kind != kPendNone)
+              if (kLabel) {
+                if (rr.kind != kPendNone) lacc += fx40((sw[0] + sw[1]) + (sw[2] + sw[3]));
+              } else if (rr.kind != kPendNone) {
                 __stcg(p.rpart + (size_t)r * p.nc + (c0 + j),
                        make_float2((sw[0] + sw[1]) + (sw[2] + sw[3]), (sp[0] + sp[1]) + (sp[2] + sp[3])));
+              }
               continue;
             }
             const int s = h * kPBaseStages + nh % kPBaseStages;
@@ -1112,6 +1143,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (lane == 0) mbar_arrive(&accEmpty[buf]);
           if (stop) break;
         }
+        if (kLabel && lacc) atomicAdd(p.lsum + pr, lacc);  // exact, order-free: deterministic
       }
       // The group never leaves the loop on one warp's say-so: every warp
       // reaches each named barrier, and the verdict written by one thread
@@ -1124,6 +1156,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       eg_sync();
       if (*sDecide) break;
+      if (kLabel) {  // every CTA's sums are in: c* = 1 - sum max(0, P - Q), and the sums back to zero
+        for (int q2 = blockIdx.x * kPEpiThreads + et; q2 < p.n_pairs; q2 += p.n_cta * kPEpiThreads) {
+          const unsigned long long v = atomicExch(p.lsum + q2, 0ull);
+          p.labels[q2] = (float)(1.0 - (double)v * 0x1p-40);
+        }
+        continue;
+      }
       for (int r = blockIdx.x; r < p.R; r += p.n_cta) {
         if (kResid)
           locate_resid_row(p, r, sA, et);
@@ -1298,6 +1337,79 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   void* args[] = {&mapW2, &mapW2, &mapA, &p};  // no base map in residual mode
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
+  launches += 1;
+  return e;
+}
+
+}  // namespace dspark
+
+namespace dspark {
+
+// The acceptance-label pass: one cooperative launch of the sweep in label
+// mode over ceil(R * gamma / 128) M tiles of (request, position) pairs. The
+// row stats of target rows 0..gamma-1 and the staged W1 rows of every pair
+// must already be in the workspace. taken = false when the shape or the device
+// does not allow it (nothing is launched).
+cudaError_t launch_label_persistent(const LabelArgs& a, cudaStream_t s, int& launches, bool& taken) {
+  taken = false;
+  DraftArgs d{a.R, a.gamma, a.V, a.rank, a.dtype, a.base, a.anchor, a.W1, a.W2, a.temperature, 0,
+              nullptr, nullptr, nullptr, a.ws};
+  if (a.temperature == 0.f || !draft_tc_eligible(d) || (reinterpret_cast<uintptr_t>(a.target) & 15) != 0)
+    return cudaSuccess;
+  int dev = 0, coop = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaSuccess;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!coop || sms <= 0) return cudaSuccess;
+  static std::atomic<unsigned long long> attr{0};
+  if (set_smem_limit_once((const void*)persistent_sweep_kernel<true, true>, (int)kPSmem, attr) != cudaSuccess)
+    return cudaSuccess;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<true, true>, kPThreads,
+                                                    kPSmem) != cudaSuccess ||
+      per_sm < 1)
+    return cudaSuccess;
+  const int n_pairs = a.R * a.gamma;
+  CUtensorMap mapW2, mapA;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.V, (uint64_t)a.rank};
+    const uint64_t strides[1] = {(uint64_t)a.V * 2};
+    const uint32_t box[2] = {64, (uint32_t)kPKC};
+    if (!make_tmap_bf16(&mapW2, a.W2, 2, dims, strides, box)) return cudaSuccess;
+  }
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  {  // staged W1 rows [R * gamma][rank] as a 3D map with a unit z extent
+    const uint64_t dims[3] = {(uint64_t)a.rank, (uint64_t)n_pairs, 1};
+    const uint64_t strides[2] = {(uint64_t)a.rank * 2, (uint64_t)n_pairs * a.rank * 2};
+    const uint32_t box[3] = {64, (uint32_t)(n_pairs < kPM ? n_pairs : kPM), 1};
+    if (!make_tmap_bf16(&mapA, ws_at<void>(a.ws, L.lstage), 3, dims, strides, box)) return cudaSuccess;
+  }
+  PersistParams p{};
+  p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
+  p.nc = ceil_div(a.V, kChunk);
+  p.n_cta = p.nc < sms ? p.nc : sms;
+  p.n_mt = ceil_div(n_pairs, kPM);
+  p.box_rows = n_pairs < kPM ? n_pairs : kPM;
+  p.greedy = 0;
+  p.kT = (float)(1.4426950408889634 / (double)a.temperature);
+  p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
+  p.base = static_cast<const __nv_bfloat16*>(a.base);
+  p.anchor = a.anchor;
+  p.q_stats = const_cast<float*>(a.q_stats);
+  p.status = ws_at<uint32_t>(a.ws, L.status);
+  p.gbar = reinterpret_cast<unsigned int*>(p.status + 1);
+  p.target = static_cast<const __nv_bfloat16*>(a.target);
+  p.rowstat = ws_at<float4>(a.ws, L.rowstat);
+  p.n_pairs = n_pairs;
+  p.lsum = ws_at<unsigned long long>(a.ws, L.lsum);
+  p.labels = a.labels;
+  taken = true;
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&mapW2, &mapW2, &mapA, &p};  // no base map in this mode
+  e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true, true>, dim3(p.n_cta), dim3(kPThreads),
+                                  args, kPSmem, s);
   launches += 1;
   return e;
 }

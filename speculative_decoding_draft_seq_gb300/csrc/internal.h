@@ -54,6 +54,20 @@ struct VerifyArgs {
   void* ws;
 };
 
+struct LabelArgs {
+  int R, gamma, V, rank, dtype;
+  const void* target;
+  const void* base;
+  const int32_t* anchor;
+  const void* W1;
+  const void* W2;
+  const int32_t* tokens;
+  const float* q_stats;
+  float temperature;
+  float* labels;
+  void* ws;
+};
+
 // Each launcher enqueues its kernels on `s`, adds the number of kernel
 // launches to `launches`, and returns cudaGetLastError().
 // Raises a kernel's dynamic shared-memory limit, once per device (devices
@@ -72,5 +86,8 @@ inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<un
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches);
+// Acceptance labels; `supported` is false (and nothing is launched) when the
+// sampled-mode shape is outside the tensor-core path.
+cudaError_t launch_labels(const LabelArgs& a, cudaStream_t s, int& launches, bool& supported);
 
 }  // namespace dspark

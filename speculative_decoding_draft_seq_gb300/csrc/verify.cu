@@ -25,6 +25,7 @@
 namespace dspark {
 
 cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& launches, bool& taken);
+bool draft_tc_eligible(const DraftArgs& a);
 
 constexpr int kRRows = 32;
 constexpr int kRKBlock = 32;
@@ -154,8 +155,8 @@ __device__ __forceinline__ void verify_row_item(
     const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, float kT, int greedy, uint64_t seed,
     float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt, float4* rowstat, float* p_tok,
     int32_t* __restrict__ out, int32_t* __restrict__ acc_len, int4* __restrict__ pend, uint32_t* status,
-    const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage, int r, int k, int sp, int L, float* shf, int* shi,
-    unsigned long long* shu, volatile int& sLast) {
+    const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage, int stats_only, int r, int k, int sp, int L,
+    float* shf, int* shi, unsigned long long* shu, volatile int& sLast) {
   const int tid = threadIdx.x;
   const size_t rowi = (size_t)r * (gamma + 1) + k;
   const size_t row = rowi * V;
@@ -256,7 +257,9 @@ __device__ __forceinline__ void verify_row_item(
       M = 0.f;
     }
     __stcg(rowstat + rowi, make_float4(M, Zf, __int_as_float(bi), 0.f));
-    if (k < L) {
+    if (stats_only) {
+      sLast = 0;  // no p, no chain: the row stats are the whole result
+    } else if (k < L) {
       int x = tokens[(size_t)r * gamma + k];
       if (x < 0 || x >= V) { set_status(status, DSPARK_ERR_RANGE); x = min(max(x, 0), V - 1); }
       float pv;
@@ -264,8 +267,10 @@ __device__ __forceinline__ void verify_row_item(
       else pv = __fdiv_rn(wgt(ld_elem(target, row + x), M), Zf);
       __stcg(p_tok + (size_t)r * gamma + k, pv);
     }
-    __threadfence();
-    sLast = atomicAdd(req_cnt + r, 1u) == (unsigned)L;  // rows 0..L of this request are combined
+    if (!stats_only) {
+      __threadfence();
+      sLast = atomicAdd(req_cnt + r, 1u) == (unsigned)L;  // rows 0..L of this request are combined
+    }
   }
   __syncthreads();
   if (!sLast || tid >= 32) return;
@@ -327,17 +332,19 @@ __global__ void __launch_bounds__(kVsThreads) verify_rows_kernel(
     const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len,
     float kT, int greedy, uint64_t seed, float4* vsplit, unsigned int* row_cnt, unsigned int* req_cnt,
     float4* rowstat, float* p_tok, int32_t* __restrict__ out, int32_t* __restrict__ acc_len,
-    int4* __restrict__ pend, uint32_t* status, const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage) {
+    int4* __restrict__ pend, uint32_t* status, const Tin* __restrict__ W1, int rank, __nv_bfloat16* astage,
+    int stats_only) {
   __shared__ float shf[32];
   __shared__ int shi[32];
   __shared__ unsigned long long shu[32];
   __shared__ int sLast;
   const int sp = blockIdx.x, r = blockIdx.y, k = blockIdx.z;
-  const int L = min(max(sched_len[r], 0), gamma);
+  // stats only (acceptance labels): rows 0..gamma-1 of every request
+  const int L = stats_only ? gamma - 1 : min(max(sched_len[r], 0), gamma);
   if (k > L) return;
   verify_row_item<Tin>(R, gamma, V, target, tokens, anchor, q_tok, kT, greedy, seed, vsplit, row_cnt, req_cnt,
-                       rowstat, p_tok, out, acc_len, pend, status, W1, rank, astage, r, k, sp, L, shf, shi, shu,
-                       sLast);
+                       rowstat, p_tok, out, acc_len, pend, status, W1, rank, astage, stats_only, r, k, sp, L, shf,
+                       shi, shu, sLast);
 }
 
 // Residual (or bonus) weight of one entry, with explicit rounding so the
@@ -532,7 +539,7 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
       a.R, a.gamma, a.V, target, a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy, a.seed,
       ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount), ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
       rowstat, a.p_tok, a.out_tokens, a.accepted_len, pend, status, W1, stage_rank,
-      ws_at<__nv_bfloat16>(ws, L.astage));
+      ws_at<__nv_bfloat16>(ws, L.astage), 0);
   launches += 1;
   if (!greedy) {
     bool taken = false;
@@ -547,6 +554,93 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
     launches += 2;
   }
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Acceptance labels of the confidence head ([GN] "Confidence head"): for every
+// request r and position k, c*_k = 1 - TV(P_{k-1}, Q_k) = 1 - sum_v max(0,
+// P_{k-1}(v) - Q_k(v)). The sampled form is one stats-only pass of
+// verify_rows_kernel over target rows 0..gamma-1, the staging of each pair's
+// W1[prev] row, and the sweep in label mode (tensor cores); the greedy form is
+// argmax agreement (the drafted token is the drafter's argmax).
+
+cudaError_t launch_label_persistent(const LabelArgs& a, cudaStream_t s, int& launches, bool& taken);
+
+// One warp per (request, position) pair: W1[prev] (prev = the anchor at k = 1,
+// else token k - 1) into the pair's staging row; 16 bytes per lane.
+__global__ void __launch_bounds__(256) label_stage_kernel(int R, int gamma, int V, int rank,
+                                                          const __nv_bfloat16* __restrict__ W1,
+                                                          const int32_t* __restrict__ anchor,
+                                                          const int32_t* __restrict__ tokens,
+                                                          __nv_bfloat16* __restrict__ lstage, uint32_t* status) {
+  const int pr = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (pr >= R * gamma) return;
+  const int r = pr / gamma, k1 = pr - r * gamma;
+  int prev = k1 == 0 ? anchor[r] : tokens[(size_t)r * gamma + k1 - 1];
+  if (prev < 0 || prev >= V) {
+    if (lane == 0) set_status(status, DSPARK_ERR_RANGE);
+    prev = min(max(prev, 0), V - 1);
+  }
+  if (8 * lane < rank)
+    reinterpret_cast<uint4*>(lstage + (size_t)pr * rank)[lane] =
+        __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)prev * rank) + lane);
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void label_greedy_kernel(int R, int gamma, const int32_t* __restrict__ tokens,
+                                    const float4* __restrict__ rowstat, float* __restrict__ labels) {
+  const int pr = blockIdx.x * blockDim.x + threadIdx.x;
+  if (pr >= R * gamma) return;
+  const int r = pr / gamma, k1 = pr - r * gamma;
+  const int tgt = __float_as_int(rowstat[(size_t)r * (gamma + 1) + k1].z);
+  labels[pr] = tokens[pr] == tgt ? 1.f : 0.f;
+}
+
+template <class Tin>
+static cudaError_t launch_labels_t(const LabelArgs& a, cudaStream_t s, int& launches, bool& supported) {
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  void* ws = a.ws;
+  const int greedy = a.temperature == 0.f;
+  supported = true;
+  if (!greedy) {  // the sampled form runs on the tensor-core path only
+    DraftArgs d{a.R, a.gamma, a.V, a.rank, a.dtype, a.base, a.anchor, a.W1, a.W2, a.temperature, 0,
+                nullptr, nullptr, nullptr, a.ws};
+    if (sizeof(Tin) != 2 || !draft_tc_eligible(d) || (reinterpret_cast<uintptr_t>(a.target) & 15) != 0) {
+      supported = false;
+      return cudaSuccess;
+    }
+  }
+  const float kT = greedy ? 0.f : (float)(1.4426950408889634 / (double)a.temperature);
+  uint32_t* status = ws_at<uint32_t>(ws, L.status);
+  float4* rowstat = ws_at<float4>(ws, L.rowstat);
+  const Tin* target = static_cast<const Tin*>(a.target);
+  const Tin* W1 = static_cast<const Tin*>(a.W1);
+  // row stats of target rows 0..gamma-1 (stats only: no p, no chains)
+  verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma), kVsThreads, 0, s>>>(
+      a.R, a.gamma, a.V, target, a.tokens, a.anchor, nullptr, nullptr, kT, greedy, 0,
+      ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount), ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
+      rowstat, nullptr, nullptr, nullptr, nullptr, status, W1, 0, nullptr, 1);
+  launches += 1;
+  const int n_pairs = a.R * a.gamma;
+  if (greedy) {
+    label_greedy_kernel<<<ceil_div(n_pairs, 256), 256, 0, s>>>(a.R, a.gamma, a.tokens, rowstat, a.labels);
+    launches += 1;
+    return cudaGetLastError();
+  }
+  label_stage_kernel<<<ceil_div(n_pairs, 8), 256, 0, s>>>(a.R, a.gamma, a.V, a.rank,
+                                                          static_cast<const __nv_bfloat16*>(a.W1), a.anchor,
+                                                          a.tokens, ws_at<__nv_bfloat16>(ws, L.lstage), status);
+  launches += 1;
+  bool taken = false;
+  cudaError_t e = launch_label_persistent(a, s, launches, taken);
+  if (e != cudaSuccess) return e;
+  if (!taken) supported = false;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_labels(const LabelArgs& a, cudaStream_t s, int& launches, bool& supported) {
+  if (a.dtype == DSPARK_BF16) return launch_labels_t<__nv_bfloat16>(a, s, launches, supported);
+  return launch_labels_t<float>(a, s, launches, supported);
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches) {

@@ -47,6 +47,8 @@ def _load():
     lib.dspark_round.restype = i32
     lib.dspark_round.argtypes = ([i32] * 5 + [vp] * 5 + [vp, vp, vp, i32, i32, f32, u64] +
                                  [vp] * 9 + [vp, sz, vp])
+    lib.dspark_acceptance_labels.restype = i32
+    lib.dspark_acceptance_labels.argtypes = [i32] * 5 + [vp] * 7 + [f32, vp, vp, sz, vp]
     lib.dspark_device_status.restype = i32
     lib.dspark_device_status.argtypes = [vp, vp]
     lib.dspark_status_string.restype = ctypes.c_char_p
@@ -137,6 +139,16 @@ def verify(target, base, anchor, W1, W2, tokens, q_tok, q_stats, sched_len, temp
                              _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(sched_len),
                              float(temperature), int(seed), _ptr(out_tokens), _ptr(accepted_len),
                              _ptr(p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_verify")
+
+
+def acceptance_labels(target, base, anchor, W1, W2, tokens, q_stats, temperature, labels, ws, stream=None):
+    """dspark_acceptance_labels: labels [R, gamma] float32 = 1 - TV(P_{k-1}, Q_k) per position."""
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_acceptance_labels(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base),
+                                        _ptr(anchor), _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_stats),
+                                        float(temperature), _ptr(labels), _ptr(ws), ws.numel(), _stream(stream)),
+           "dspark_acceptance_labels")
 
 
 def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,

@@ -25,7 +25,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("dspark_draft_sequential", "dspark_schedule", "dspark_verify", "dspark_round",
-              "dspark_workspace_bytes", "dspark_device_status", "dspark_status_string"):
+              "dspark_acceptance_labels", "dspark_workspace_bytes", "dspark_device_status",
+              "dspark_status_string"):
         assert n in names
 
 
@@ -44,6 +45,9 @@ def test_host_only_calls(lib):
     # argument errors are returned before anything touches the GPU
     lib.dspark_schedule.restype = ctypes.c_int32
     assert lib.dspark_schedule(0, 4, None, None, None, 0, 0, None, None, None, None, 0, None) == 1
+    lib.dspark_acceptance_labels.restype = ctypes.c_int32
+    assert lib.dspark_acceptance_labels(0, 4, 100, 64, 1, *([None] * 7), ctypes.c_float(1.0), None, None,
+                                        ctypes.c_size_t(0), None) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

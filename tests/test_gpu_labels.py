@@ -1,0 +1,76 @@
+"""GPU parity of the acceptance labels (1 - TV(P_{k-1}, Q_k) per drafted
+position) against the oracle, on the same drafted tokens."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+from oracle import labels as Lb
+from oracle.draft import decode
+
+pytestmark = pytest.mark.gpu
+
+LABEL_ATOL = 2e-5
+
+
+def _device_labels(cfg, inp):
+    from speculative_decoding_draft_seq_gb300 import dspark
+    R, gamma, V = inp["base"].shape
+    dt = dspark.BF16 if inp["base"].dtype == torch.bfloat16 else dspark.FP32
+    ws = dspark.new_workspace(R, gamma, V, inp["W1"].shape[1], dt, inp["sps"].numel())
+    out = dspark.RoundOutputs(R, gamma)
+    dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"], out.tokens,
+                            out.q_tok, out.q_stats, ws)
+    labels = torch.full((R, gamma), -1.0, dtype=torch.float32, device=inp["base"].device)
+    dspark.acceptance_labels(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], out.tokens,
+                             out.q_stats, inp["T"], labels, ws)
+    assert dspark.device_status(ws) == dspark.OK
+    return out.tokens.cpu().numpy(), labels.cpu().numpy(), dspark.last_launch_count()
+
+
+def _oracle_labels(cfg, tokens, requests):
+    o = W.oracle_inputs(cfg, requests)
+    W1f = decode(o["W1"]).astype(np.float64)
+    W2f = decode(o["W2"]).astype(np.float64)
+    return {r: Lb.position_labels(decode(o["target"][r]), decode(o["base"][r]), int(o["anchor"][r]), W1f, W2f,
+                                  tokens[r], cfg.T) for r in requests}
+
+
+SHAPES = [W.Workload("lab_tc", R=150, gamma=4, V=3000, rank=64, dtype="bf16", T=1.0, mode=W.CAUSAL, seed=5001,
+                     base_sd=1.5, w_sd=0.05, target_sd=(0.45,), conf_law="decreasing", table="concave",
+                     n_table=750),
+          W.Workload("lab_small", R=9, gamma=7, V=2056, rank=256, dtype="bf16", T=0.7, mode=W.CAUSAL, seed=5002,
+                     base_sd=1.5, w_sd=0.05, target_sd=(1.0,), conf_law="decreasing", table="concave",
+                     n_table=72)]
+
+
+@pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
+def test_labels_match_oracle(cfg):
+    inp = W.device_inputs(cfg, "cuda")
+    tokens, lab, launches = _device_labels(cfg, inp)
+    ref = _oracle_labels(cfg, tokens, list(range(cfg.R)))
+    for r in range(cfg.R):
+        np.testing.assert_allclose(lab[r], ref[r], rtol=0, atol=LABEL_ATOL)
+    assert launches == 3  # stats, staging, one tensor-core sweep
+
+
+@pytest.mark.parametrize("cfg", [W.with_(s, T=0.0) for s in SHAPES], ids=[c.name + "_greedy" for c in SHAPES])
+def test_greedy_labels_are_exact(cfg):
+    inp = W.device_inputs(cfg, "cuda")
+    tokens, lab, _ = _device_labels(cfg, inp)
+    ref = _oracle_labels(cfg, tokens, list(range(cfg.R)))
+    for r in range(cfg.R):
+        np.testing.assert_array_equal(lab[r], ref[r].astype(np.float32))
+
+
+def test_labels_full_size_sampled():
+    """DeepSeek-scale (R = 128, gamma = 16, V = 129280): every label in [0, 1],
+    and sampled requests (first, middle, last) against the oracle."""
+    cfg = W.CONFIGS["ds"]
+    inp = W.device_inputs(cfg, "cuda")
+    tokens, lab, _ = _device_labels(cfg, inp)
+    assert np.all((lab >= 0) & (lab <= 1))
+    ref = _oracle_labels(cfg, tokens, [0, 64, 127])
+    for r, v in ref.items():
+        np.testing.assert_allclose(lab[r], v, rtol=0, atol=LABEL_ATOL)
