@@ -141,6 +141,13 @@ class ClockSampler:
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_ds_round.md")
 
 
+def label_bytes(cfg):
+    """Distinct bytes the acceptance-label pass must read: target rows 0..gamma-1, the base
+    rows, W2 once and the W1 rows of the drafted tokens."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    return (2 * cfg.R * cfg.gamma * cfg.V + cfg.rank * cfg.V + cfg.R * cfg.gamma * cfg.rank) * e
+
+
 def csrc_digest():
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_draft_seq_gb300", "csrc")
@@ -282,6 +289,14 @@ def main():
                                                 inp["W2"], out.tokens, out.q_tok, out.q_stats, out.sched_len,
                                                 inp["T"], inp["seed"], out.out_tokens, out.accepted_len,
                                                 out.p_tok, ws), max(3, args.steps // 4))
+    # the acceptance-label pass (training signal of the confidence head; not part of the round)
+    labels = torch.empty((R, gamma), dtype=torch.float32, device=dev)
+    try:  # the sampled form needs the tensor-core shape
+        t_labels = time_stage(lambda: dspark.acceptance_labels(inp["target"], inp["base"], inp["anchor"], inp["W1"],
+                                                               inp["W2"], out.tokens, out.q_stats, inp["T"], labels,
+                                                               ws), max(3, args.steps // 8))
+    except dspark.DSparkError:
+        t_labels = None
 
     clocks = ClockSampler()
     if world > 1:
@@ -356,6 +371,10 @@ def main():
         "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
+        "labels": None if t_labels is None else {
+            "us": t_labels * 1e3, "algorithmic_bytes": label_bytes(cfg),
+            "achieved_gbs": label_bytes(cfg) / (t_labels * 1e-3) / 1e9,
+            "frac": label_bytes(cfg) / (t_labels * 1e-3) / 1e9 / peak},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": ach / peak,
                      "traffic": traffic,
