@@ -246,6 +246,36 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
                            float* p_tok, void* workspace, size_t workspace_bytes,
                            dspark_stream_t stream);
 
+/*
+ * Sequential Temperature Scaling of the confidence head (GeekNews page,
+ * "Calibração posterior — Sequential Temperature Scaling (STS)").
+ *
+ * dspark_sts_fit: on a held-out set of N blocks with confidences
+ * conf [N, gamma] float and A = accepted [N] int32 (leading drafted tokens that
+ * passed verification, every position verified), finds per-position
+ * temperatures left to right: T_k is the first value of grid [n_grid] that
+ * minimises the expected calibration error (n_bins equal-width bins on [0, 1],
+ * sum over bins of |sum of predictions - sum of outcomes| / N) of the
+ * calibrated survival prod_{i<=k} sigmoid(logit(c_i) / T_i) against the outcome
+ * [A >= k], T_1..T_{k-1} fixed. Confidences are clipped to [1e-6, 1 - 1e-6]
+ * before the logit. Writes temperature [gamma] and, unless NULL, the ECE curve
+ * ece [gamma, n_grid]. n_bins is at most 64. scratch: device memory of
+ * dspark_sts_scratch_bytes(...) bytes, 256-byte aligned, owned by the caller;
+ * a non-finite confidence sets DSPARK_ERR_NONFINITE in it, read by
+ * dspark_sts_status (which synchronises the stream).
+ *
+ * dspark_sts_apply: conf_out[r, k] = sigmoid(logit(clip(conf[r, k])) / T_k),
+ * the calibrated confidences to pass to dspark_schedule (non-finite inputs
+ * are passed through, for the scheduler to report).
+ */
+size_t dspark_sts_scratch_bytes(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins);
+dspark_status dspark_sts_fit(int32_t N, int32_t gamma, const float* conf, const int32_t* accepted,
+                             int32_t n_grid, const float* grid, int32_t n_bins, float* temperature, float* ece,
+                             void* scratch, size_t scratch_bytes, dspark_stream_t stream);
+dspark_status dspark_sts_status(const void* scratch, dspark_stream_t stream);
+dspark_status dspark_sts_apply(int32_t R, int32_t gamma, const float* conf, const float* temperature,
+                               float* conf_out, dspark_stream_t stream);
+
 /* Synchronises `stream`, then returns the workspace's sticky device status
  * (DSPARK_OK if no device-side error was recorded). */
 dspark_status dspark_device_status(const void* workspace, dspark_stream_t stream);

@@ -49,6 +49,14 @@ def _load():
                                  [vp] * 9 + [vp, sz, vp])
     lib.dspark_acceptance_labels.restype = i32
     lib.dspark_acceptance_labels.argtypes = [i32] * 5 + [vp] * 7 + [f32, vp, vp, sz, vp]
+    lib.dspark_sts_scratch_bytes.restype = sz
+    lib.dspark_sts_scratch_bytes.argtypes = [i32] * 4
+    lib.dspark_sts_fit.restype = i32
+    lib.dspark_sts_fit.argtypes = [i32, i32, vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
+    lib.dspark_sts_status.restype = i32
+    lib.dspark_sts_status.argtypes = [vp, vp]
+    lib.dspark_sts_apply.restype = i32
+    lib.dspark_sts_apply.argtypes = [i32, i32, vp, vp, vp, vp]
     lib.dspark_device_status.restype = i32
     lib.dspark_device_status.argtypes = [vp, vp]
     lib.dspark_status_string.restype = ctypes.c_char_p
@@ -149,6 +157,26 @@ def acceptance_labels(target, base, anchor, W1, W2, tokens, q_stats, temperature
                                         _ptr(anchor), _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_stats),
                                         float(temperature), _ptr(labels), _ptr(ws), ws.numel(), _stream(stream)),
            "dspark_acceptance_labels")
+
+
+def sts_fit(conf, accepted, grid, n_bins, temperature, ece=None, stream=None):
+    """dspark_sts_fit with a scratch it allocates (PyTorch); returns the device status."""
+    N, gamma = conf.shape
+    n = int(lib.dspark_sts_scratch_bytes(N, gamma, grid.numel(), n_bins))
+    if n == 0:
+        raise DSparkError(ERR_INVALID_ARG, "dspark_sts_scratch_bytes")
+    raw = torch.empty(n + 256, dtype=torch.uint8, device=conf.device)
+    off = (-raw.data_ptr()) % 256
+    scratch = raw[off:off + n]
+    _check(lib.dspark_sts_fit(N, gamma, _ptr(conf), _ptr(accepted), grid.numel(), _ptr(grid), n_bins,
+                              _ptr(temperature), _ptr(ece), _ptr(scratch), n, _stream(stream)), "dspark_sts_fit")
+    return int(lib.dspark_sts_status(_ptr(scratch), _stream(stream)))
+
+
+def sts_apply(conf, temperature, conf_out, stream=None):
+    R, gamma = conf.shape
+    _check(lib.dspark_sts_apply(R, gamma, _ptr(conf), _ptr(temperature), _ptr(conf_out), _stream(stream)),
+           "dspark_sts_apply")
 
 
 def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,
