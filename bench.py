@@ -298,6 +298,21 @@ def main():
     except dspark.DSparkError:
         t_labels = None
 
+    # Sequential Temperature Scaling (offline calibration of the confidences): a held-out set of
+    # 65,536 blocks x gamma drawn from over-confident scores, 64 grid temperatures, 15 bins
+    n_sts = 65536
+    g_sts = torch.Generator(device="cpu").manual_seed(7)
+    z_sts = torch.randn((n_sts, gamma), generator=g_sts, dtype=torch.float64) * 1.5 + 1.0
+    c_sts = torch.sigmoid(z_sts).float().to(dev)
+    passed = torch.rand((n_sts, gamma), generator=g_sts, dtype=torch.float64) < torch.sigmoid(0.6 * z_sts)
+    first_fail = torch.where(passed.all(dim=1), torch.full((n_sts,), gamma), (~passed).int().argmax(dim=1))
+    a_sts = first_fail.int().to(dev)
+    grid_sts = torch.exp(torch.linspace(np.log(0.25), np.log(4.0), 64, dtype=torch.float64)).float().to(dev)
+    t_sts = torch.zeros(gamma, dtype=torch.float32, device=dev)
+    t_sts_fit = time_stage(lambda: dspark.sts_fit(c_sts, a_sts, grid_sts, 15, t_sts), 3)
+    conf_cal = torch.empty_like(inp["conf"])
+    t_sts_apply = time_stage(lambda: dspark.sts_apply(inp["conf"], t_sts, conf_cal), 5)
+
     clocks = ClockSampler()
     if world > 1:
         torch.distributed.barrier()
@@ -371,6 +386,8 @@ def main():
         "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
+        "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
+                "apply_us": t_sts_apply * 1e3},
         "labels": None if t_labels is None else {
             "us": t_labels * 1e3, "algorithmic_bytes": label_bytes(cfg),
             "achieved_gbs": label_bytes(cfg) / (t_labels * 1e-3) / 1e9,
