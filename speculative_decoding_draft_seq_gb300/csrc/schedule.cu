@@ -399,15 +399,23 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   unsigned long long* fxl = fxv + kRankMaxKeys;
   uint32_t* key = reinterpret_cast<uint32_t*>(fxl + kRankMaxKeys);
   uint32_t* keyl = key + kRankMaxKeys;
-  __shared__ int sLast, sBad;
+  __shared__ int sLast;
   __shared__ unsigned long long sMax[kRankThreads / 32];
   __shared__ int sMaxI[kRankThreads / 32];
   unsigned int* done = status + 2;
   unsigned long long* all_sum = reinterpret_cast<unsigned long long*>(status + 4);
   unsigned int* stop_enc = status + 6;
+  unsigned int* bad_table = status + 8;
   const int tid = threadIdx.x, T = blockDim.x;
   const int n = R * gamma;
   const bool lagged = mode == DSPARK_SCHED_LAGGED;
+  {  // this CTA's slice of the cost table must be finite
+    const int per = ceil_div(n_table, (int)gridDim.x);
+    const int j0 = (int)blockIdx.x * per, j1 = min(j0 + per, n_table);
+    bool badv = false;
+    for (int j = j0 + tid; j < j1; j += T) badv |= !isfinite(__ldg(sps + j));
+    if (badv) atomicOr(bad_table, 1u);
+  }
 
   survival_keys_smem(conf, R, gamma, key, fxv, status);
   if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, fxl, status);
@@ -453,24 +461,17 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   __threadfence();
 
   // admission (last CTA)
-  if (tid == 0) sBad = 0;
-  __syncthreads();
-  {
-    bool bad = false;
-#pragma unroll 8
-    for (int j = tid; j < n_table; j += T) bad |= !isfinite(__ldg(sps + j));
-    if (bad) sBad = 1;
-  }
-  __syncthreads();
   const unsigned long long total = __ldcg(all_sum);
   const unsigned int enc = __ldcg(stop_enc);
+  const unsigned int bad = __ldcg(bad_table);
   __syncthreads();
   if (tid == 0) {  // every counter back to zero for the next call
     *done = 0u;
     *all_sum = 0ull;
     *stop_enc = 0u;
+    *bad_table = 0u;
   }
-  if (sBad) {
+  if (bad) {
     if (tid == 0) {
       set_status(status, DSPARK_ERR_NONFINITE);
       *Kout = 0;
@@ -524,14 +525,20 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   } else {
     K = enc ? n - (int)enc : n;
   }
+  // the prefix at K (thread 0) and the positions (every thread) are fetched together
+  unsigned long long S = 0ull;
+  float sps_K = 0.f;
   if (tid == 0) {
-    const unsigned long long S = K ? __ldcg(prefix_g + (K - 1)) : 0ull;
-    *Kout = K;
-    tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
-    tau_theta[1] = theta_of(R, S, sps[R + K - 1]);
+    S = K ? __ldcg(prefix_g + (K - 1)) : 0ull;
+    sps_K = __ldg(sps + R + K - 1);
   }
   uint32_t* srank = key;  // the positions, staged over the key array
   stage_smem(srank, pos_g, n);
+  if (tid == 0) {
+    *Kout = K;
+    tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
+    tau_theta[1] = theta_of(R, S, sps_K);
+  }
   __syncthreads();
   for (int r = tid; r < R; r += T) {
     int cnt = 0;
@@ -543,9 +550,9 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
 // Both scheduler forms behind one call: the many-CTA rank kernel (admission
 // in its last CTA) for small problems, the single-CTA radix sort otherwise.
 // Scratch: key0/key1/idx0/idx1 (u32[n] each), fx (u64[n]), for the small form
-// fx2 (u64[n]); status[0] is the sticky status word, status[2], [4..5] and
-// [6] the small form's completion counter, sum and stop word (zero between
-// calls).
+// fx2 (u64[n]); status[0] is the sticky status word, status[2], [4..5], [6]
+// and [8] the small form's completion counter, sum, stop word and cost-table
+// flag (zero between calls).
 cudaError_t schedule_launch(const ScheduleArgs& a, uint32_t* key0, uint32_t* key1, uint32_t* idx0, uint32_t* idx1,
                             unsigned long long* fx, unsigned long long* fx2, uint32_t* status, cudaStream_t s,
                             int& launches) {
