@@ -82,8 +82,13 @@ class DraftDist:
     gap (infinite for T > 0) so a flipped argmax can be attributed.
     """
 
-    def __init__(self, base_row_f32, prev, W1f, W2f, T):
-        bias = markov_bias(W1f, W2f, prev)
+    def __init__(self, base_row_f32, prev, W1f, W2f, T, a_row=None):
+        # a_row: the head's operand row when it is not W1[prev] (the gated
+        # head's rounded state, oracle/gated.py); the bias is a_row . W2
+        if a_row is None:
+            bias = markov_bias(W1f, W2f, prev)
+        else:
+            bias = np.asarray(a_row, dtype=np.float64) @ np.asarray(W2f, dtype=np.float64)
         V = base_row_f32.shape[0]
         if T == 0.0:
             l32 = base_row_f32 + bias.astype(np.float32)  # fl32(base + fl32(bias))

@@ -66,10 +66,13 @@ class TargetDist:
         return self.w / self.Z
 
 
-def verify_request(target_r, base_r, anchor, W1f, W2f, tokens, L, T, seed, r):
+def verify_request(target_r, base_r, anchor, W1f, W2f, tokens, L, T, seed, r, a_rows=None):
     """Verify the first L draft tokens of request r.
 
     target_r [gamma+1, V] float32, base_r [gamma, V] float32, tokens [gamma].
+    a_rows [gamma, rank]: the head's operand rows when the head is not the
+    Markov head (oracle/gated.py state_rows); Q_k is then recomputed from
+    a_rows[k-1] . W2.
     Returns dict(A, out [A+1] tokens emitted, p [L] = P_{k-1}(x_k),
     q [L] = Q_k(x_k), margins list of (kind, k, distance), new_token).
     """
@@ -81,7 +84,8 @@ def verify_request(target_r, base_r, anchor, W1f, W2f, tokens, L, T, seed, r):
     Qs = []
     prev = int(anchor)
     for k in range(1, L + 1):
-        Qs.append(DraftDist(base_r[k - 1], prev, W1f, W2f, T))
+        Qs.append(DraftDist(base_r[k - 1], prev, W1f, W2f, T,
+                            a_row=None if a_rows is None else a_rows[k - 1]))
         prev = int(tokens[k - 1])
     for k in range(1, L + 1):
         x = int(tokens[k - 1])

@@ -11,12 +11,15 @@ with its exact probability (to the bisection width, 1e-14).
 """
 import numpy as np
 
-from oracle import draft as D, verify as Vf, philox
+from oracle import draft as D, verify as Vf, gated as G, philox
 
 EPS = 1e-15
 
 
-def run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script):
+def run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script, gate=None):
+    """One request through the oracle's draft and verification with scripted
+    uniforms; `gate` (float32 gate values [V, rank]) selects the gated head,
+    whose W1 must then hold float32 (bf16-valued) rows."""
     calls = []
 
     def stub(seed, r, k, purpose):
@@ -26,9 +29,15 @@ def run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script):
 
     monkeypatch.setattr(D, "uniform", stub)
     monkeypatch.setattr(Vf, "uniform", stub)
-    d = D.draft_request(base_r, anchor, W1, W2, T, seed=0, r=0)
+    monkeypatch.setattr(G, "uniform", stub)
+    if gate is None:
+        d = D.draft_request(base_r, anchor, W1, W2, T, seed=0, r=0)
+        a_rows = None
+    else:
+        d = G.draft_request_gated(base_r, anchor, W1, gate, W2, T, seed=0, r=0)
+        a_rows = G.state_rows(anchor, d["tokens"], W1, gate)
     L = L_of(d["tokens"])
-    v = Vf.verify_request(target_r, base_r, anchor, W1, W2, d["tokens"], L, T, seed=0, r=0)
+    v = Vf.verify_request(target_r, base_r, anchor, W1, W2, d["tokens"], L, T, seed=0, r=0, a_rows=a_rows)
     return calls, d["tokens"], v
 
 
@@ -41,12 +50,12 @@ def _observe(call, tokens, v):
     return int(v["new_token"])
 
 
-def law(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of):
+def law(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, gate=None):
     """dict: emitted tuple -> probability, plus dict: draft tuple -> probability."""
     out = {}
 
     def obs(script, n):
-        calls, tokens, v = run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script)
+        calls, tokens, v = run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script, gate)
         return _observe(calls[n], tokens, v)
 
     def segments(script, n):
@@ -70,7 +79,7 @@ def law(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of):
         return [(edges[i], edges[i + 1]) for i in range(len(edges) - 1)]
 
     def dfs(script, weight):
-        calls, tokens, v = run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script)
+        calls, tokens, v = run(monkeypatch, base_r, target_r, anchor, W1, W2, T, L_of, script, gate)
         n = len(script)
         if len(calls) == n:
             key = tuple(int(x) for x in v["out"])

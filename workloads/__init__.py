@@ -37,6 +37,7 @@ _MUL_B = 0x2C1B3C6D
 
 # Tensor stream salts.
 S_BASE, S_EXTRA, S_TARGET, S_W1, S_W2 = 0x1B873593, 0x5BD1E995, 0x27D4EB2F, 0x165667B1, 0x61C88647
+S_GATE = 0x3C6EF372
 
 CAUSAL, LAGGED, ALL = 0, 1, 2
 
@@ -60,6 +61,8 @@ class Workload:
     conf_law: str = "decreasing"
     table: str = "concave"
     n_table: int = 0
+    gated: bool = False         # the recurrent (gated) head: gate values [V, rank] in [gate_lo, 1]
+    gate_lo: float = 0.25
     notes: str = ""
 
     @property
@@ -223,6 +226,20 @@ def weights_np(cfg):
     return _finish_np(cfg, w1)[0], _finish_np(cfg, w2)[0]
 
 
+def _gate_f32_np(cfg):
+    """Gate values lo + (1 - lo) u, u = 24 hash bits * 2^-24 (exact in float32),
+    one float32 multiply and one add."""
+    idx = np.arange(cfg.V * cfg.rank, dtype=np.uint64)
+    h = _hash_np(idx, _salt(cfg, S_GATE))
+    u = (h >> 8).astype(np.float32) * np.float32(2.0 ** -24)
+    return (np.float32(cfg.gate_lo) + np.float32(1.0 - cfg.gate_lo) * u).astype(np.float32).reshape(cfg.V, cfg.rank)
+
+
+def gate_np(cfg):
+    """Gate values [V, rank] of the gated head, as stored (bf16 bits or float32)."""
+    return _finish_np(cfg, _gate_f32_np(cfg))[0]
+
+
 # ----------------------------------------------------------------------------
 # small host tensors (PCG64)
 
@@ -295,6 +312,8 @@ def oracle_inputs(cfg, requests=None):
     W1, W2 = weights_np(cfg)
     d = host_inputs(cfg)
     d.update(W1=W1, W2=W2)
+    if cfg.gated:
+        d["gate"] = gate_np(cfg)
     d["base"] = {r: base[i] for i, r in enumerate(reqs)}
     d["target"] = {r: tgt[i] for i, r in enumerate(reqs)}
     return d
@@ -385,6 +404,16 @@ def weights_device(cfg, device):
     return w1.contiguous(), w2.contiguous()
 
 
+def gate_device(cfg, device):
+    torch = _torch()
+    idx = torch.arange(cfg.V * cfg.rank, dtype=torch.int64, device=device)
+    h = _hash_t(idx, _salt(cfg, S_GATE))
+    u = (h >> 8).to(torch.float32) * torch.tensor(2.0 ** -24, dtype=torch.float32, device=device)
+    lo = torch.tensor(cfg.gate_lo, dtype=torch.float32, device=device)
+    one_m = torch.tensor(1.0 - cfg.gate_lo, dtype=torch.float32, device=device)
+    return _finish_t(cfg, lo + one_m * u).reshape(cfg.V, cfg.rank).contiguous()
+
+
 def device_inputs(cfg, device="cuda"):
     """Every input of one round as device tensors (torch), for the library."""
     torch = _torch()
@@ -394,4 +423,4 @@ def device_inputs(cfg, device="cuda"):
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
     return dict(base=base, target=target, W1=W1, W2=W2, anchor=t(h["anchor"]), conf=t(h["conf"]),
                 conf_lag=t(h["conf_lag"]), sps=t(h["sps"]), T=cfg.T, seed=cfg.philox_seed,
-                mode=cfg.mode)
+                mode=cfg.mode, gate=gate_device(cfg, device) if cfg.gated else None)
