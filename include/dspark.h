@@ -247,6 +247,57 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
                            dspark_stream_t stream);
 
 /*
+ * Recurrent (gated) sequential head (GeekNews page, "Geração
+ * semiautorregressiva": "Head RNN", the variant that keeps a recurrent state
+ * of the whole prefix drafted in the block, updated through gates). The pages
+ * give no equations; the reading implemented is a minimal gated recurrence
+ * over the head's input, the previous token prev_k (the anchor at k = 1,
+ * else x_{k-1}):
+ *   s_0 = 0,  s_k = (1 - gate[prev_k]) * s_{k-1} + gate[prev_k] * W1[prev_k]
+ * elementwise in float32 (each product and sum rounded once), and
+ *   bias_k = bf16(s_k) . W2      (s_k rounded to bf16, ties to even).
+ * gate [V, rank] (dtype, values in [0, 1]) is the update gate of each token,
+ * tabulated once (a gate driven by a one-hot input is a row lookup). Gate
+ * values 1 give the Markov head exactly; 0 gives bias 0.
+ *
+ * dspark_draft_sequential_gated, dspark_verify_gated and dspark_round_gated
+ * take the arguments of dspark_draft_sequential, dspark_verify and
+ * dspark_round plus `gate` (after W1), and write the same outputs;
+ * verification recomputes the residual's Q_j from the state replayed over the
+ * anchor and the accepted tokens. They run on the tensor-core path only:
+ * dtype BF16, rank a multiple of 64 up to 256, V a multiple of 8 and at least
+ * 64, every tensor 16-byte aligned, and a device with cooperative launch;
+ * otherwise they return DSPARK_ERR_INVALID_ARG and enqueue nothing. The
+ * workspace is the same as for the Markov head (it holds each request's
+ * float32 state between steps).
+ */
+dspark_status dspark_draft_sequential_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank,
+                                            int32_t dtype, const void* base_logits,
+                                            const int32_t* anchor, const void* W1, const void* gate,
+                                            const void* W2, float temperature, uint64_t seed,
+                                            int32_t* draft_tokens, float* q_tok, float* q_stats,
+                                            void* workspace, size_t workspace_bytes,
+                                            dspark_stream_t stream);
+dspark_status dspark_verify_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                  const void* target_logits, const void* base_logits,
+                                  const int32_t* anchor, const void* W1, const void* gate,
+                                  const void* W2, const int32_t* draft_tokens, const float* q_tok,
+                                  const float* q_stats, const int32_t* sched_len,
+                                  float temperature, uint64_t seed, int32_t* out_tokens,
+                                  int32_t* accepted_len, float* p_tok, void* workspace,
+                                  size_t workspace_bytes, dspark_stream_t stream);
+dspark_status dspark_round_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                 const void* base_logits, const void* target_logits,
+                                 const int32_t* anchor, const void* W1, const void* gate,
+                                 const void* W2, const float* conf, const float* conf_lagged,
+                                 const float* sps_table, int32_t n_table, int32_t mode,
+                                 float temperature, uint64_t seed, int32_t* draft_tokens,
+                                 float* q_tok, float* q_stats, int32_t* sched_len, int32_t* K,
+                                 double* tau_theta, int32_t* out_tokens, int32_t* accepted_len,
+                                 float* p_tok, void* workspace, size_t workspace_bytes,
+                                 dspark_stream_t stream);
+
+/*
  * Sequential Temperature Scaling of the confidence head (GeekNews page,
  * "Calibração posterior — Sequential Temperature Scaling (STS)").
  *

@@ -59,11 +59,14 @@ dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes, dsp
   return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
 }
 
-dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
-                                      const void* base_logits, const int32_t* anchor, const void* W1,
-                                      const void* W2, float temperature, uint64_t seed,
-                                      int32_t* draft_tokens, float* q_tok, float* q_stats,
-                                      void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+}  // extern "C"
+
+// Drafting with the Markov head (gate == nullptr) or the gated head.
+static dspark_status draft_entry(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                 const void* base_logits, const int32_t* anchor, const void* W1, const void* gate,
+                                 const void* W2, float temperature, uint64_t seed, int32_t* draft_tokens,
+                                 float* q_tok, float* q_stats, void* workspace, size_t workspace_bytes,
+                                 dspark_stream_t stream) {
   g_last_launches = 0;
   if (!dims_ok(R, gamma, V, rank, dtype) || !(temperature >= 0.f) || !isfinite(temperature))
     return DSPARK_ERR_INVALID_ARG;
@@ -71,11 +74,40 @@ dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32
     return DSPARK_ERR_INVALID_ARG;
   if (!ws_ok(workspace, workspace_bytes, ws_layout(R, gamma, V).total)) return DSPARK_ERR_WORKSPACE;
   DraftArgs a{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, temperature, seed,
-              draft_tokens, q_tok, q_stats, workspace};
+              draft_tokens, q_tok, q_stats, workspace, gate};
   int n = 0;
-  cudaError_t e = launch_draft(a, (cudaStream_t)stream, n);
+  cudaError_t e;
+  if (gate) {  // the persistent tensor-core sweep only: decide before enqueueing anything
+    if (!gated_supported(a)) return DSPARK_ERR_INVALID_ARG;
+    bool taken = false;
+    e = launch_draft_persistent(a, (cudaStream_t)stream, n, taken);
+    if (e == cudaSuccess && !taken) return DSPARK_ERR_INVALID_ARG;
+  } else {
+    e = launch_draft(a, (cudaStream_t)stream, n);
+  }
   g_last_launches = n;
   return cuda_status(e);
+}
+
+extern "C" {
+
+dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                      const void* base_logits, const int32_t* anchor, const void* W1,
+                                      const void* W2, float temperature, uint64_t seed,
+                                      int32_t* draft_tokens, float* q_tok, float* q_stats,
+                                      void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+  return draft_entry(R, gamma, V, rank, dtype, base_logits, anchor, W1, nullptr, W2, temperature, seed,
+                     draft_tokens, q_tok, q_stats, workspace, workspace_bytes, stream);
+}
+
+dspark_status dspark_draft_sequential_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                            const void* base_logits, const int32_t* anchor, const void* W1,
+                                            const void* gate, const void* W2, float temperature, uint64_t seed,
+                                            int32_t* draft_tokens, float* q_tok, float* q_stats,
+                                            void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+  if (!gate) return DSPARK_ERR_INVALID_ARG;
+  return draft_entry(R, gamma, V, rank, dtype, base_logits, anchor, W1, gate, W2, temperature, seed,
+                     draft_tokens, q_tok, q_stats, workspace, workspace_bytes, stream);
 }
 
 dspark_status dspark_schedule(int32_t R, int32_t gamma, const float* conf, const float* conf_lagged,
@@ -97,12 +129,25 @@ dspark_status dspark_schedule(int32_t R, int32_t gamma, const float* conf, const
   return cuda_status(e);
 }
 
-dspark_status dspark_verify(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
-                            const void* target_logits, const void* base_logits, const int32_t* anchor,
-                            const void* W1, const void* W2, const int32_t* draft_tokens,
-                            const float* q_tok, const float* q_stats, const int32_t* sched_len,
-                            float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accepted_len,
-                            float* p_tok, void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+}  // extern "C"
+
+// The gated head's support check for verification: its residual draw runs
+// only on the tensor-core sweep, which reads the target rows with 16-byte
+// copies, so the drafting conditions plus an aligned target tensor.
+static bool gated_verify_supported(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                   const void* target_logits, const void* base_logits, const int32_t* anchor,
+                                   const void* W1, const void* gate, const void* W2, void* workspace) {
+  DraftArgs d{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, 1.f, 0, nullptr, nullptr, nullptr,
+              workspace, gate};
+  return gated_supported(d) && (reinterpret_cast<uintptr_t>(target_logits) & 15) == 0;
+}
+
+static dspark_status verify_entry(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                  const void* target_logits, const void* base_logits, const int32_t* anchor,
+                                  const void* W1, const void* gate, const void* W2, const int32_t* draft_tokens,
+                                  const float* q_tok, const float* q_stats, const int32_t* sched_len,
+                                  float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accepted_len,
+                                  float* p_tok, void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
   g_last_launches = 0;
   if (!dims_ok(R, gamma, V, rank, dtype) || !(temperature >= 0.f) || !isfinite(temperature))
     return DSPARK_ERR_INVALID_ARG;
@@ -110,22 +155,52 @@ dspark_status dspark_verify(int32_t R, int32_t gamma, int32_t V, int32_t rank, i
       !sched_len || !out_tokens || !accepted_len || !p_tok)
     return DSPARK_ERR_INVALID_ARG;
   if (!ws_ok(workspace, workspace_bytes, ws_layout(R, gamma, V).total)) return DSPARK_ERR_WORKSPACE;
+  if (gate && !gated_verify_supported(R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, gate, W2,
+                                      workspace))
+    return DSPARK_ERR_INVALID_ARG;
   VerifyArgs a{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens,
-               q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace};
+               q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace, gate};
   int n = 0;
   cudaError_t e = launch_verify(a, (cudaStream_t)stream, n);
   g_last_launches = n;
   return cuda_status(e);
 }
 
-dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
-                           const void* base_logits, const void* target_logits, const int32_t* anchor,
-                           const void* W1, const void* W2, const float* conf, const float* conf_lagged,
-                           const float* sps_table, int32_t n_table, int32_t mode, float temperature,
-                           uint64_t seed, int32_t* draft_tokens, float* q_tok, float* q_stats,
-                           int32_t* sched_len, int32_t* K, double* tau_theta, int32_t* out_tokens,
-                           int32_t* accepted_len, float* p_tok, void* workspace, size_t workspace_bytes,
-                           dspark_stream_t stream) {
+extern "C" {
+
+dspark_status dspark_verify(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                            const void* target_logits, const void* base_logits, const int32_t* anchor,
+                            const void* W1, const void* W2, const int32_t* draft_tokens,
+                            const float* q_tok, const float* q_stats, const int32_t* sched_len,
+                            float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accepted_len,
+                            float* p_tok, void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+  return verify_entry(R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, nullptr, W2,
+                      draft_tokens, q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok,
+                      workspace, workspace_bytes, stream);
+}
+
+dspark_status dspark_verify_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                  const void* target_logits, const void* base_logits, const int32_t* anchor,
+                                  const void* W1, const void* gate, const void* W2, const int32_t* draft_tokens,
+                                  const float* q_tok, const float* q_stats, const int32_t* sched_len,
+                                  float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accepted_len,
+                                  float* p_tok, void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+  if (!gate) return DSPARK_ERR_INVALID_ARG;
+  return verify_entry(R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, gate, W2, draft_tokens,
+                      q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace,
+                      workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+static dspark_status round_entry(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                 const void* base_logits, const void* target_logits, const int32_t* anchor,
+                                 const void* W1, const void* gate, const void* W2, const float* conf,
+                                 const float* conf_lagged, const float* sps_table, int32_t n_table, int32_t mode,
+                                 float temperature, uint64_t seed, int32_t* draft_tokens, float* q_tok,
+                                 float* q_stats, int32_t* sched_len, int32_t* K, double* tau_theta,
+                                 int32_t* out_tokens, int32_t* accepted_len, float* p_tok, void* workspace,
+                                 size_t workspace_bytes, dspark_stream_t stream) {
   g_last_launches = 0;
   if (!dims_ok(R, gamma, V, rank, dtype) || !(temperature >= 0.f) || !isfinite(temperature))
     return DSPARK_ERR_INVALID_ARG;
@@ -137,22 +212,61 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
     return DSPARK_ERR_INVALID_ARG;
   if (!ws_ok(workspace, workspace_bytes, dspark_workspace_bytes(R, gamma, V, rank, dtype, n_table)))
     return DSPARK_ERR_WORKSPACE;
+  if (gate && !gated_verify_supported(R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, gate, W2,
+                                      workspace))
+    return DSPARK_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int n = 0;
   DraftArgs da{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, temperature, seed,
-               draft_tokens, q_tok, q_stats, workspace};
-  cudaError_t e = launch_draft(da, s, n);
+               draft_tokens, q_tok, q_stats, workspace, gate};
+  cudaError_t e;
+  if (gate) {
+    bool taken = false;
+    e = launch_draft_persistent(da, s, n, taken);
+    if (e == cudaSuccess && !taken) return DSPARK_ERR_INVALID_ARG;  // nothing was enqueued
+  } else {
+    e = launch_draft(da, s, n);
+  }
   if (e == cudaSuccess) {
     ScheduleArgs sa{R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta, workspace};
     e = launch_schedule(sa, s, n);
   }
   if (e == cudaSuccess) {
     VerifyArgs va{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens,
-                  q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace};
+                  q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace, gate};
     e = launch_verify(va, s, n);
   }
   g_last_launches = n;
   return cuda_status(e);
+}
+
+extern "C" {
+
+dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                           const void* base_logits, const void* target_logits, const int32_t* anchor,
+                           const void* W1, const void* W2, const float* conf, const float* conf_lagged,
+                           const float* sps_table, int32_t n_table, int32_t mode, float temperature,
+                           uint64_t seed, int32_t* draft_tokens, float* q_tok, float* q_stats,
+                           int32_t* sched_len, int32_t* K, double* tau_theta, int32_t* out_tokens,
+                           int32_t* accepted_len, float* p_tok, void* workspace, size_t workspace_bytes,
+                           dspark_stream_t stream) {
+  return round_entry(R, gamma, V, rank, dtype, base_logits, target_logits, anchor, W1, nullptr, W2, conf,
+                     conf_lagged, sps_table, n_table, mode, temperature, seed, draft_tokens, q_tok, q_stats,
+                     sched_len, K, tau_theta, out_tokens, accepted_len, p_tok, workspace, workspace_bytes, stream);
+}
+
+dspark_status dspark_round_gated(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
+                                 const void* base_logits, const void* target_logits, const int32_t* anchor,
+                                 const void* W1, const void* gate, const void* W2, const float* conf,
+                                 const float* conf_lagged, const float* sps_table, int32_t n_table, int32_t mode,
+                                 float temperature, uint64_t seed, int32_t* draft_tokens, float* q_tok,
+                                 float* q_stats, int32_t* sched_len, int32_t* K, double* tau_theta,
+                                 int32_t* out_tokens, int32_t* accepted_len, float* p_tok, void* workspace,
+                                 size_t workspace_bytes, dspark_stream_t stream) {
+  if (!gate) return DSPARK_ERR_INVALID_ARG;
+  return round_entry(R, gamma, V, rank, dtype, base_logits, target_logits, anchor, W1, gate, W2, conf,
+                     conf_lagged, sps_table, n_table, mode, temperature, seed, draft_tokens, q_tok, q_stats,
+                     sched_len, K, tau_theta, out_tokens, accepted_len, p_tok, workspace, workspace_bytes, stream);
 }
 
 dspark_status dspark_acceptance_labels(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,

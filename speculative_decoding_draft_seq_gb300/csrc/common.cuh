@@ -29,6 +29,7 @@ struct WsLayout {
   size_t pend;     // int4   [R]             (kind, target row, prev token, accepted)
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
+  size_t gcarry;   // float  [R][256]        gated head: float32 state of each request between steps
   size_t vsplit;   // float4 [R][gamma+1][4] target row quarter stats (M_s, Z_s, max, argmax)
   size_t vcount;   // u32    [R*(gamma+1) + R] row / request completion counters (zero between calls)
   size_t lstage;   // bf16   [R*gamma][256]  acceptance labels: W1 rows of every (request, position)
@@ -53,6 +54,7 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.rowstat = o; o = align256(o + (size_t)R * (gamma + 1) * sizeof(float4));
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
   L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
+  L.gcarry = o;  o = align256(o + (size_t)R * 256 * sizeof(float));
   L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * 4 * sizeof(float4));
   L.lstage = o;  o = align256(o + (size_t)R * gamma * 256 * 2);
   L.lsum = o;    o = align256(o + (size_t)R * gamma * sizeof(unsigned long long));
@@ -85,6 +87,32 @@ __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, size_t i) {
   return __uint_as_float(((uint32_t)b) << 16);
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// ---------------------------------------------------------------------------
+// Recurrent (gated) sequential head ("Head RNN" of the GeekNews page): state
+// s_k = (1 - z[prev_k]) * s_{k-1} + z[prev_k] * W1[prev_k] elementwise, s_0 = 0,
+// in float32 with each operation rounded once (z * w of two bf16 values is
+// exact); the operand row of position k is s_k rounded to bf16 (to nearest,
+// ties to even). Eight elements per call, packed as 16 bytes of bf16 pairs
+// (element 2e in the low half of word e).
+__device__ __forceinline__ void gated_update8(float s[8], const uint4& z, const uint4& w) {
+  const uint32_t zz[4] = {z.x, z.y, z.z, z.w}, ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float z0 = __uint_as_float(zz[e] << 16), z1 = __uint_as_float(zz[e] & 0xffff0000u);
+    const float w0 = __uint_as_float(ww[e] << 16), w1 = __uint_as_float(ww[e] & 0xffff0000u);
+    s[2 * e] = __fadd_rn(__fmul_rn(__fsub_rn(1.f, z0), s[2 * e]), __fmul_rn(z0, w0));
+    s[2 * e + 1] = __fadd_rn(__fmul_rn(__fsub_rn(1.f, z1), s[2 * e + 1]), __fmul_rn(z1, w1));
+  }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float s[8]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    o[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s[2 * e])) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s[2 * e + 1])) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // ---------------------------------------------------------------------------
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of the 4x64

@@ -81,6 +81,9 @@ struct PersistParams {
   float2* part;
   unsigned int* gbar;  // grid-barrier counter, zero at launch
   __nv_bfloat16* astage;  // [2][R][rank] W1 rows of the drawn tokens, by step parity
+  // recurrent (gated) head: astage holds bf16(s_k) instead of W1[prev]
+  const __nv_bfloat16* gate;  // [V, rank] gate values in [0, 1]; null for the Markov head
+  float* gcarry;              // [R][256] float32 state s_k of each request between steps
   uint32_t* status;
   // residual / bonus pass of verification
   const __nv_bfloat16* target;  // [R, gamma+1, V]
@@ -225,6 +228,38 @@ __device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_
 
 namespace dspark {
 
+// Gated head, eight state elements per lane: s_k of request r at step k
+// (k = 1: z[anchor] * W1[anchor], exact; else the state the previous step
+// left in gcarry, written by this same thread).
+__device__ __forceinline__ void gated_state_k(const PersistParams& p, int r, int k, int lane, float gs[8]) {
+  if (k == 1) {
+    const int a = min(max(__ldg(p.anchor + r), 0), p.V - 1);
+    const uint4 z = __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)a * p.rank) + lane);
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)a * p.rank) + lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) gs[e] = 0.f;
+    gated_update8(gs, z, w);
+  } else {
+    const float4* c = reinterpret_cast<const float4*>(p.gcarry + (size_t)r * 256) + 2 * lane;
+    const float4 x = __ldcg(c), y = __ldcg(c + 1);
+    gs[0] = x.x; gs[1] = x.y; gs[2] = x.z; gs[3] = x.w;
+    gs[4] = y.x; gs[5] = y.y; gs[6] = y.z; gs[7] = y.w;
+  }
+}
+__device__ __forceinline__ void store_gcarry(const PersistParams& p, int r, int lane, const float gs[8]) {
+  float4* c = reinterpret_cast<float4*>(p.gcarry + (size_t)r * 256) + 2 * lane;
+  __stcg(c, make_float4(gs[0], gs[1], gs[2], gs[3]));
+  __stcg(c + 1, make_float4(gs[4], gs[5], gs[6], gs[7]));
+}
+// s_{k+1} = update(s_k, z[tok], W1[tok]); the carry and the staged bf16 row.
+__device__ __forceinline__ void gated_advance(const PersistParams& p, int r, int tok, int lane, float gs[8],
+                                              const uint4& wv, uint4* stage) {
+  const uint4 zv = __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)tok * p.rank) + lane);
+  gated_update8(gs, zv, wv);
+  store_gcarry(p, r, lane, gs);
+  stage[lane] = pack_bf16x8(gs);
+}
+
 // Draws token k of request r from the chunk partials (epilogue group of 256
 // threads, et = thread index in the group). `ls` is the locate scratch. When a
 // step k + 1 follows, the W1 row of the drawn token is staged in
@@ -281,7 +316,14 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     eg_argmax(bv, bi, shf, shi2, ew, lane);
     const int tok = min(max(bi, 0), p.V - 1);
     if (ew == 0 && stage_next && 8 * lane < p.rank) {  // 16 bytes of the W1 row per lane
-      stage[lane] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)tok * p.rank) + lane);
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)tok * p.rank) + lane);
+      if (p.gate) {
+        float gs[8];
+        gated_state_k(p, r, k, lane, gs);
+        gated_advance(p, r, tok, lane, gs, wv, stage);
+      } else {
+        stage[lane] = wv;
+      }
       fence_proxy_async_global();
     }
     if (et == 0) {
@@ -298,7 +340,12 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
   // CTA staged when it drew token k - 1 of this request
   if (k == 1) {
     const int a = min(max(__ldg(p.anchor + r), 0), p.V - 1);
-    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)a * p.rank + i]);
+    for (int i = et; i < p.rank; i += kPEpiThreads) {
+      const float w = __bfloat162float(p.W1[(size_t)a * p.rank + i]);
+      // gated head: s_1 = z[anchor] * W1[anchor] (exact), rounded to bf16
+      sW1f[i] = p.gate ? __bfloat162float(__float2bfloat16_rn(__fmul_rn(__bfloat162float(p.gate[(size_t)a * p.rank + i]), w)))
+                       : w;
+    }
   } else {
     const __nv_bfloat16* prev_row = p.astage + ((size_t)((k - 1) & 1) * p.R + r) * p.rank;
     for (int i = et; i < p.rank; i += kPEpiThreads) {
@@ -419,7 +466,11 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     const uint32_t bytes = (uint32_t)(min(kChunk, p.V - colbase) * p.rank * 2);
     mbar_expect_tx(w1Full, bytes);
     bulk_load(ls + kLsW1Blk, p.W1 + (size_t)colbase * p.rank, bytes, w1Full);
+    if (p.gate) bulk_prefetch_l2(p.gate + (size_t)colbase * p.rank, bytes);  // the candidates' gate rows
   }
+  // gated head: this step's state, read while the chunk is recomputed
+  float gs[8];
+  if (p.gate && stage_next && ew == 0 && 8 * lane < p.rank) gated_state_k(p, r, k, lane, gs);
   // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   float bcol = 0.f;
   if (et < kChunk && colbase + et < p.V)
@@ -485,9 +536,18 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     }
     const int tok = min(colbase + xc, p.V - 1);
     if (stage_next) {  // copy W1[tok] from the fetched chunk rows to the staging row
+      uint4 zv = make_uint4(0, 0, 0, 0);
+      if (p.gate && 8 * lane < p.rank) zv = __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)tok * p.rank) + lane);
       mbar_wait_drain(w1Full, w1_use & 1, p.status);
       if (8 * lane < p.rank) {
-        stage[lane] = *reinterpret_cast<const uint4*>(sBlk + (size_t)(tok - colbase) * p.rank * 2 + 16 * lane);
+        const uint4 wv = *reinterpret_cast<const uint4*>(sBlk + (size_t)(tok - colbase) * p.rank * 2 + 16 * lane);
+        if (p.gate) {
+          gated_update8(gs, zv, wv);
+          store_gcarry(p, r, lane, gs);
+          stage[lane] = pack_bf16x8(gs);
+        } else {
+          stage[lane] = wv;
+        }
         fence_proxy_async_global();
       }
     }
@@ -668,10 +728,10 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
 
   const ResidRow rr = load_resid_row(p, r);
   if (rr.kind == kPendNone) return;  // same for every thread of the group
-  const int4 pd = __ldg(p.pend + r);
-  const int prev = min(max(pd.z, 0), p.V - 1);
-  if (rr.kind == kPendResid)
-    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __bfloat162float(p.W1[(size_t)prev * p.rank + i]);
+  if (rr.kind == kPendResid) {  // the A row the verifier staged: W1[prev], or bf16(s_j) for the gated head
+    const unsigned short* arow = reinterpret_cast<const unsigned short*>(p.astage + (size_t)r * p.rank);
+    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __uint_as_float((uint32_t)__ldcg(arow + i) << 16);
+  }
 
   const int nc = p.nc;
   const float2* pr = p.rpart + (size_t)r * nc;
@@ -1011,14 +1071,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
           }
           const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)max(prev, 0) * p.rank);
-          uint4 val[16];
+          if (p.gate) {  // gated head: s_1 = z[anchor] * W1[anchor] (exact), rounded to bf16
+            const uint4* zsrc = reinterpret_cast<const uint4*>(p.gate + (size_t)max(prev, 0) * p.rank);
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              uint4 wv[8], zv[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            val[i] = (prev >= 0 && 8 * (j0 + i) < p.rank) ? __ldg(src + j0 + i) : make_uint4(0, 0, 0, 0);
+              for (int i = 0; i < 8; ++i) {
+                const int j = j0 + 8 * hh + i;
+                const bool ok = prev >= 0 && 8 * j < p.rank;
+                wv[i] = ok ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+                zv[i] = ok ? __ldg(zsrc + j) : make_uint4(0, 0, 0, 0);
+              }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = j0 + i, kc = j >> 3, uu = j & 7;
-            *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val[i];
+              for (int i = 0; i < 8; ++i) {
+                const int j = j0 + 8 * hh + i, kc = j >> 3, uu = j & 7;
+                float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                gated_update8(s8, zv[i], wv[i]);
+                *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = pack_bf16x8(s8);
+              }
+            }
+          } else {
+            uint4 val[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              val[i] = (prev >= 0 && 8 * (j0 + i) < p.rank) ? __ldg(src + j0 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = j0 + i, kc = j >> 3, uu = j & 7;
+              *reinterpret_cast<uint4*>(sA + kc * kPAChunk + m * 128 + ((uu ^ (m & 7)) << 4)) = val[i];
+            }
           }
           fence_proxy_async_smem();
           eg_sync();
@@ -1259,6 +1341,8 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   p.status = ws_at<uint32_t>(a.ws, L.status);
   p.gbar = reinterpret_cast<unsigned int*>(p.status + 1);
   p.astage = ws_at<__nv_bfloat16>(a.ws, L.astage);
+  p.gate = static_cast<const __nv_bfloat16*>(a.gate);
+  p.gcarry = ws_at<float>(a.ws, L.gcarry);
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
@@ -1272,6 +1356,14 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
 }  // namespace dspark
 
 namespace dspark {
+
+bool gated_supported(const DraftArgs& a) {
+  if (!a.gate || !draft_tc_eligible(a) || (reinterpret_cast<uintptr_t>(a.gate) & 15) != 0) return false;
+  int dev = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  return coop != 0;
+}
 
 // The verifier's residual / bonus draw on the tensor cores: one cooperative
 // launch of the sweep kernel in residual mode. Returns taken = false (and
@@ -1331,6 +1423,7 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   p.rowstat = ws_at<float4>(a.ws, L.rowstat);
   p.out_tokens = a.out_tokens;
   p.rpart = ws_at<float2>(a.ws, L.rpart);
+  p.astage = ws_at<__nv_bfloat16>(a.ws, L.astage);
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;

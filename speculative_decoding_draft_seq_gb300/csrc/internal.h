@@ -21,6 +21,7 @@ struct DraftArgs {
   float* q_tok;
   float* q_stats;
   void* ws;
+  const void* gate = nullptr;  // gated head: gate values [V, rank] (bf16); null = Markov head
 };
 
 struct ScheduleArgs {
@@ -52,6 +53,7 @@ struct VerifyArgs {
   int32_t* accepted_len;
   float* p_tok;
   void* ws;
+  const void* gate = nullptr;  // gated head: gate values [V, rank] (bf16); null = Markov head
 };
 
 struct LabelArgs {
@@ -84,6 +86,10 @@ inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<un
 }
 
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches);
+// The gated head runs only on the persistent tensor-core path: bf16, rank a
+// multiple of 64 up to 256, V a multiple of 8 and at least 64, 16-byte
+// aligned tensors, cooperative launch.
+bool gated_supported(const DraftArgs& a);
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches);
 // Acceptance labels; `supported` is false (and nothing is launched) when the

@@ -4,17 +4,22 @@
 // the longest prefix consistent with the target distribution; decoding-cycle
 // paragraph: E and F accepted, G rejected, corrected token G* emitted).
 //
-// Four launches:
-//   verify_stats   one CTA per scheduled target row (r, k <= L_r): streams the
-//                  row once with 128-bit loads, online max / sum of
-//                  2^((t - m) log2(e) / T) per thread, float64 block combine;
-//                  writes (M, Z, argmax) and p_tok = P_k(x_{k+1}).
-//   verify_chain   one thread per request: ratio tests u < p / q in order;
-//                  first rejection j = A + 1 -> residual draw, otherwise the
-//                  bonus draw from row L_r = A. Both use target row A.
+// Launches:
+//   verify_rows_kernel  one CTA per quarter of each scheduled target row
+//                  (r, k <= L_r): streams it once with 128-bit loads (online
+//                  max / sum of 2^((t - m) log2(e) / T)); the last quarter of a
+//                  row combines the four (M, Z, argmax) and writes
+//                  p_tok = P_k(x_{k+1}); the last row of a request runs its
+//                  chain of ratio tests u < p / q, records the pending
+//                  residual (first rejection j = A + 1) or bonus draw (row
+//                  L_r = A), and stages the A row of the residual's Q_j.
+//   gated_stage_kernel  (recurrent head only) the A row bf16(s_j), the state
+//                  replayed over the anchor and the accepted tokens.
+//   the residual / bonus draw: the tensor-core sweep in residual mode
+//                  (draft_persistent.cu) or, for shapes it does not take,
 //   resid_partials per (64-column chunk, 32 requests): residual weights
 //                  max(0, P - Q) (Q recomputed with the Markov bias of the
-//                  rejected position) or bonus weights P, chunk sums.
+//                  rejected position) or bonus weights P, chunk sums, and
 //   resid_locate   one CTA per request: float64 scan of chunk sums, inverse
 //                  CDF, recompute of the crossing chunk, emitted token.
 #include <algorithm>
@@ -519,6 +524,50 @@ __global__ void __launch_bounds__(256) resid_locate_kernel(
   }
 }
 
+// Recurrent (gated) head: the A row of request r's residual draw at the
+// first rejected position j = A + 1 is bf16(s_j), s_j the state after the
+// anchor and the accepted tokens x_1..x_A (the same float32 recurrence as the
+// drafting kernel); zeros for a bonus draw. One CTA per request, one thread
+// per state element; the gate and W1 rows of eight positions are loaded
+// together.
+__global__ void __launch_bounds__(256) gated_stage_kernel(int R, int gamma, int V, int rank,
+                                                          const int32_t* __restrict__ anchor,
+                                                          const int32_t* __restrict__ tokens,
+                                                          const __nv_bfloat16* __restrict__ W1,
+                                                          const __nv_bfloat16* __restrict__ gate,
+                                                          const int4* __restrict__ pend,
+                                                          __nv_bfloat16* astage) {
+  __shared__ int sPrev[8];
+  const int r = blockIdx.x, e = threadIdx.x;
+  const int4 pd = pend[r];
+  const bool resid = pd.x == kPendResid;
+  const int A = resid ? min(max(pd.w, 0), gamma - 1) : -1;
+  float st = 0.f;
+  for (int i0 = 0; i0 <= A; i0 += 8) {
+    __syncthreads();
+    if (e < 8 && i0 + e <= A) {
+      const int t = i0 + e == 0 ? anchor[r] : tokens[(size_t)r * gamma + i0 + e - 1];
+      sPrev[e] = min(max(t, 0), V - 1);
+    }
+    __syncthreads();
+    if (e < rank) {
+      float z[8], w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool ok = i0 + u <= A;
+        const size_t o = (size_t)(ok ? sPrev[u] : 0) * rank + e;
+        z[u] = ok ? ld_elem(gate, o) : 0.f;
+        w[u] = ok ? ld_elem(W1, o) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u <= A) st = __fadd_rn(__fmul_rn(__fsub_rn(1.f, z[u]), st), __fmul_rn(z[u], w[u]));
+    }
+  }
+  if (e < rank) astage[(size_t)r * rank + e] = resid ? __float2bfloat16_rn(st) : __float2bfloat16_rn(0.f);
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 template <class Tin>
 static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& launches) {
   const WsLayout L = ws_layout(a.R, a.gamma, a.V);
@@ -533,7 +582,8 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
   const Tin* base = static_cast<const Tin*>(a.base);
   const Tin* W1 = static_cast<const Tin*>(a.W1);
   const Tin* W2 = static_cast<const Tin*>(a.W2);
-  const int stage_rank = (sizeof(Tin) == 2 && a.rank % 64 == 0 && a.rank <= 256 &&
+  // the chain stages W1[prev] for the Markov head; the gated head's rows come next
+  const int stage_rank = (sizeof(Tin) == 2 && !a.gate && a.rank % 64 == 0 && a.rank <= 256 &&
                           (reinterpret_cast<uintptr_t>(a.W1) & 15) == 0) ? a.rank : 0;
   verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma + 1), kVsThreads, 0, s>>>(
       a.R, a.gamma, a.V, target, a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy, a.seed,
@@ -542,9 +592,19 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& lau
       ws_at<__nv_bfloat16>(ws, L.astage), 0);
   launches += 1;
   if (!greedy) {
+    if (a.gate) {
+      gated_stage_kernel<<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, a.anchor, a.tokens,
+                                             static_cast<const __nv_bfloat16*>(a.W1),
+                                             static_cast<const __nv_bfloat16*>(a.gate), pend,
+                                             ws_at<__nv_bfloat16>(ws, L.astage));
+      launches += 1;
+    }
     bool taken = false;
     cudaError_t e = launch_resid_persistent(a, s, launches, taken);
     if (taken || e != cudaSuccess) return e == cudaSuccess ? cudaGetLastError() : e;
+    // the fallback kernels below recompute the Markov bias; the gated head
+    // was admitted only where the tensor-core pass runs
+    if (a.gate) return cudaErrorNotSupported;
     const int nc = ceil_div(a.V, kChunk);
     resid_partials_kernel<Tin><<<dim3(nc, ceil_div(a.R, kRRows)), 256, 0, s>>>(
         a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats, rowstat, pend, kT, rpart);

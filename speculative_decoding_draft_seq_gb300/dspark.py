@@ -47,6 +47,13 @@ def _load():
     lib.dspark_round.restype = i32
     lib.dspark_round.argtypes = ([i32] * 5 + [vp] * 5 + [vp, vp, vp, i32, i32, f32, u64] +
                                  [vp] * 9 + [vp, sz, vp])
+    lib.dspark_draft_sequential_gated.restype = i32
+    lib.dspark_draft_sequential_gated.argtypes = [i32] * 5 + [vp] * 5 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
+    lib.dspark_verify_gated.restype = i32
+    lib.dspark_verify_gated.argtypes = [i32] * 5 + [vp] * 10 + [f32, u64] + [vp] * 3 + [vp, sz, vp]
+    lib.dspark_round_gated.restype = i32
+    lib.dspark_round_gated.argtypes = ([i32] * 5 + [vp] * 6 + [vp, vp, vp, i32, i32, f32, u64] +
+                                       [vp] * 9 + [vp, sz, vp])
     lib.dspark_acceptance_labels.restype = i32
     lib.dspark_acceptance_labels.argtypes = [i32] * 5 + [vp] * 7 + [f32, vp, vp, sz, vp]
     lib.dspark_sts_scratch_bytes.restype = sz
@@ -122,6 +129,17 @@ def draft_sequential(base, anchor, W1, W2, temperature, seed, tokens, q_tok, q_s
            "dspark_draft_sequential")
 
 
+def draft_sequential_gated(base, anchor, W1, gate, W2, temperature, seed, tokens, q_tok, q_stats, ws,
+                           stream=None):
+    """Drafting with the recurrent (gated) head; `gate` [V, rank] like W1."""
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_draft_sequential_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor),
+                                             _ptr(W1), _ptr(gate), _ptr(W2), float(temperature), int(seed),
+                                             _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(ws), ws.numel(),
+                                             _stream(stream)), "dspark_draft_sequential_gated")
+
+
 def schedule(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, ws, stream=None):
     R, gamma = conf.shape
     _check(lib.dspark_schedule(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(), int(mode),
@@ -147,6 +165,17 @@ def verify(target, base, anchor, W1, W2, tokens, q_tok, q_stats, sched_len, temp
                              _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(sched_len),
                              float(temperature), int(seed), _ptr(out_tokens), _ptr(accepted_len),
                              _ptr(p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_verify")
+
+
+def verify_gated(target, base, anchor, W1, gate, W2, tokens, q_tok, q_stats, sched_len, temperature, seed,
+                 out_tokens, accepted_len, p_tok, ws, stream=None):
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_verify_gated(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base),
+                                   _ptr(anchor), _ptr(W1), _ptr(gate), _ptr(W2), _ptr(tokens), _ptr(q_tok),
+                                   _ptr(q_stats), _ptr(sched_len), float(temperature), int(seed),
+                                   _ptr(out_tokens), _ptr(accepted_len), _ptr(p_tok), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "dspark_verify_gated")
 
 
 def acceptance_labels(target, base, anchor, W1, W2, tokens, q_stats, temperature, labels, ws, stream=None):
@@ -190,6 +219,19 @@ def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperatu
                             _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K), _ptr(out.tau_theta),
                             _ptr(out.out_tokens), _ptr(out.accepted_len), _ptr(out.p_tok), _ptr(ws),
                             ws.numel(), _stream(stream)), "dspark_round")
+
+
+def round_gated(base, target, anchor, W1, gate, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,
+                stream=None):
+    """One whole round with the recurrent (gated) head."""
+    R, gamma, V = base.shape
+    rank = W1.shape[1]
+    _check(lib.dspark_round_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target), _ptr(anchor),
+                                  _ptr(W1), _ptr(gate), _ptr(W2), _ptr(conf), _ptr(conf_lagged), _ptr(sps),
+                                  sps.numel(), int(mode), float(temperature), int(seed), _ptr(out.tokens),
+                                  _ptr(out.q_tok), _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K),
+                                  _ptr(out.tau_theta), _ptr(out.out_tokens), _ptr(out.accepted_len),
+                                  _ptr(out.p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_round_gated")
 
 
 def device_status(ws, stream=None):

@@ -31,8 +31,12 @@ def gpu_round(cfg, inp=None, device="cuda"):
     dt = dspark.BF16 if inp["base"].dtype == torch.bfloat16 else dspark.FP32
     ws = dspark.new_workspace(R, gamma, V, rank, dt, inp["sps"].numel(), device)
     out = dspark.RoundOutputs(R, gamma, device)
-    dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
-                  inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+    if inp.get("gate") is not None:  # the recurrent (gated) head
+        dspark.round_gated(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["gate"], inp["W2"],
+                           inp["conf"], inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+    else:
+        dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                      inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
     status = dspark.device_status(ws)
     res = out.host()
     res["status"] = status

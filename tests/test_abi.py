@@ -26,7 +26,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("dspark_draft_sequential", "dspark_schedule", "dspark_verify", "dspark_round",
               "dspark_acceptance_labels", "dspark_workspace_bytes", "dspark_device_status",
-              "dspark_status_string"):
+              "dspark_status_string", "dspark_draft_sequential_gated", "dspark_verify_gated",
+              "dspark_round_gated"):
         assert n in names
 
 
@@ -48,6 +49,17 @@ def test_host_only_calls(lib):
     lib.dspark_acceptance_labels.restype = ctypes.c_int32
     assert lib.dspark_acceptance_labels(0, 4, 100, 64, 1, *([None] * 7), ctypes.c_float(1.0), None, None,
                                         ctypes.c_size_t(0), None) == 1
+    # the gated entry points refuse a missing gate table on the host
+    f = ctypes.c_float(1.0)
+    lib.dspark_draft_sequential_gated.restype = ctypes.c_int32
+    assert lib.dspark_draft_sequential_gated(4, 4, 128, 64, 1, *([None] * 5), f, ctypes.c_uint64(0),
+                                             None, None, None, None, ctypes.c_size_t(0), None) == 1
+    lib.dspark_verify_gated.restype = ctypes.c_int32
+    assert lib.dspark_verify_gated(4, 4, 128, 64, 1, *([None] * 10), f, ctypes.c_uint64(0),
+                                   None, None, None, None, ctypes.c_size_t(0), None) == 1
+    lib.dspark_round_gated.restype = ctypes.c_int32
+    assert lib.dspark_round_gated(4, 4, 128, 64, 1, *([None] * 9), ctypes.c_int32(0), ctypes.c_int32(0), f,
+                                  ctypes.c_uint64(0), *([None] * 10), ctypes.c_size_t(0), None) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -1,0 +1,93 @@
+"""GPU parity of the recurrent (gated) sequential head ([GN] "Head RNN")
+against the oracle, through the C ABI: the same parity contract as the Markov
+head (tokens and lengths bit-exact but for counted boundary decisions,
+probabilities within 2e-3 relative, greedy fully bit-exact)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_harness import compare, device_inputs, gpu_round, oracle_round
+    from speculative_decoding_draft_seq_gb300 import dspark
+
+GATED = [
+    # (R, gamma, V, rank): several chunks per CTA, a vocabulary tail, two M tiles
+    (33, 6, 640, 256),
+    (150, 4, 3000, 64),
+    (200, 3, 2056, 128),
+    (64, 5, 4104, 192),
+]
+
+
+def _cfg(R, gamma, V, rank, T, **kw):
+    return W.Workload(f"gated_{R}_{gamma}_{V}_{rank}", R=R, gamma=gamma, V=V, rank=rank, dtype="bf16", T=T,
+                      mode=W.CAUSAL, seed=5000 + R + gamma + rank, base_sd=1.5, w_sd=0.05,
+                      target_sd=(0.45,), conf_law="decreasing", table="concave", n_table=R * (gamma + 1),
+                      gated=True, **kw)
+
+
+@pytest.mark.parametrize("R,gamma,V,rank", GATED)
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_gated_round_parity(R, gamma, V, rank, T):
+    cfg = _cfg(R, gamma, V, rank, T)
+    g = gpu_round(cfg)
+    o = oracle_round(cfg, list(range(R)))
+    rep = compare(cfg, g, o, list(range(R)))
+    assert rep["positions"] > 0
+    # draft sweep, scheduler, row stats, and (sampled) the state staging and the residual sweep
+    assert g["launches"] == (5 if T > 0 else 3), g["launches"]
+
+
+def test_gated_uses_the_prefix():
+    """With gates well below 1 the drafted tokens differ from the Markov
+    head's on the same inputs (the state carries earlier tokens)."""
+    cfg = _cfg(64, 6, 2048, 128, 1.0, gate_lo=0.1)
+    inp = device_inputs(cfg)
+    g = gpu_round(cfg, inp)
+    m = gpu_round(cfg, dict(inp, gate=None))
+    assert not np.array_equal(g["tokens"], m["tokens"])
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_gate_one_equals_the_markov_round(T):
+    """Gate values 1: the gated path on the device gives the Markov head's
+    round bit for bit (every output)."""
+    cfg = _cfg(96, 5, 3000, 128, T)
+    inp = device_inputs(cfg)
+    ones = torch.ones_like(inp["W1"])
+    g = gpu_round(cfg, dict(inp, gate=ones))
+    m = gpu_round(cfg, dict(inp, gate=None))
+    for key in ("tokens", "q_tok", "q_stats", "sched_len", "out_tokens", "accepted_len", "p_tok"):
+        assert np.array_equal(g[key], m[key]), key
+
+
+def test_gated_full_size_sampled():
+    """The DeepSeek-scale round with the gated head, sampled requests against
+    the oracle."""
+    cfg = W.with_(W.CONFIGS["ds"], gated=True)
+    requests = [0, 64, 127]
+    g = gpu_round(cfg)
+    o = oracle_round(cfg, requests)
+    rep = compare(cfg, g, o, requests)
+    rep = {k: (float(v) if isinstance(v, (float, np.floating)) else v) for k, v in rep.items()}
+    out_dir = os.environ.get("DSPARK_OUT_DIR", "runs")
+    os.makedirs(out_dir, exist_ok=True)
+    with open(os.path.join(out_dir, "parity_reports.jsonl"), "a") as f:
+        f.write(json.dumps({"workload": "ds_gated", "T": cfg.T, "requests": requests, **rep}) + "\n")
+
+
+def test_gated_refuses_shapes_off_the_tensor_core_path():
+    cfg = W.Workload("gated_fp32", R=4, gamma=3, V=130, rank=5, dtype="fp32", T=1.0, mode=W.CAUSAL, seed=7,
+                     zipf=0.0, w_sd=0.4, n_table=16, gated=True)
+    inp = device_inputs(cfg)
+    with pytest.raises(dspark.DSparkError) as e:
+        gpu_round(cfg, inp)
+    assert e.value.status == dspark.ERR_INVALID_ARG
