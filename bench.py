@@ -313,6 +313,26 @@ def main():
     conf_cal = torch.empty_like(inp["conf"])
     t_sts_apply = time_stage(lambda: dspark.sts_apply(inp["conf"], t_sts, conf_cal), 5)
 
+    # the recurrent (gated) head: the same workload with a gate table [V, rank]
+    gated = None
+    if cfg.dtype == "bf16":
+        gate = W.gate_device(W.with_(cfg, gated=True), dev)
+        gout = dspark.RoundOutputs(R, gamma, dev)
+        try:
+            t_gdraft = time_stage(lambda: dspark.draft_sequential_gated(
+                inp["base"], inp["anchor"], inp["W1"], gate, inp["W2"], inp["T"], inp["seed"], gout.tokens,
+                gout.q_tok, gout.q_stats, ws), max(3, args.steps // 8))
+            t_ground = time_stage(lambda: dspark.round_gated(
+                inp["base"], inp["target"], inp["anchor"], inp["W1"], gate, inp["W2"], inp["conf"],
+                inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], gout, ws), max(3, args.steps // 8))
+            if dspark.device_status(ws) != dspark.OK:
+                raise RuntimeError("device status after the gated rounds")
+            gb = algorithmic_bytes(cfg, np.zeros(R, dtype=np.int64))[0] + R * gamma * cfg.rank * 2  # + gate rows
+            gated = {"round_us": t_ground * 1e3, "draft_us": t_gdraft * 1e3, "draft_algorithmic_bytes": gb,
+                     "draft_frac": gb / (t_gdraft * 1e-3) / 1e9 / peaks()[0]}
+        except dspark.DSparkError:
+            gated = None
+
     clocks = ClockSampler()
     if world > 1:
         torch.distributed.barrier()
@@ -388,6 +408,7 @@ def main():
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
+        "gated_head": gated,
         "labels": None if t_labels is None else {
             "us": t_labels * 1e3, "algorithmic_bytes": label_bytes(cfg),
             "achieved_gbs": label_bytes(cfg) / (t_labels * 1e-3) / 1e9,

@@ -266,6 +266,7 @@ __device__ __forceinline__ void gated_advance(const PersistParams& p, int r, int
 // astage[k & 1][r], the A-operand row of request r for that step; the 64 W1
 // rows of the crossing chunk are fetched into shared memory (bulk copy counted
 // on w1Full, use number w1_use) while the chunk's logits are recomputed.
+template <bool kGated>
 __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* ls, int et, uint64_t* w1Full,
                            uint32_t& w1_use) {
   const int ew = et >> 5, lane = et & 31;
@@ -317,7 +318,7 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     const int tok = min(max(bi, 0), p.V - 1);
     if (ew == 0 && stage_next && 8 * lane < p.rank) {  // 16 bytes of the W1 row per lane
       const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)tok * p.rank) + lane);
-      if (p.gate) {
+      if (kGated) {
         float gs[8];
         gated_state_k(p, r, k, lane, gs);
         gated_advance(p, r, tok, lane, gs, wv, stage);
@@ -343,7 +344,7 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     for (int i = et; i < p.rank; i += kPEpiThreads) {
       const float w = __bfloat162float(p.W1[(size_t)a * p.rank + i]);
       // gated head: s_1 = z[anchor] * W1[anchor] (exact), rounded to bf16
-      sW1f[i] = p.gate ? __bfloat162float(__float2bfloat16_rn(__fmul_rn(__bfloat162float(p.gate[(size_t)a * p.rank + i]), w)))
+      sW1f[i] = kGated ? __bfloat162float(__float2bfloat16_rn(__fmul_rn(__bfloat162float(p.gate[(size_t)a * p.rank + i]), w)))
                        : w;
     }
   } else {
@@ -466,11 +467,11 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     const uint32_t bytes = (uint32_t)(min(kChunk, p.V - colbase) * p.rank * 2);
     mbar_expect_tx(w1Full, bytes);
     bulk_load(ls + kLsW1Blk, p.W1 + (size_t)colbase * p.rank, bytes, w1Full);
-    if (p.gate) bulk_prefetch_l2(p.gate + (size_t)colbase * p.rank, bytes);  // the candidates' gate rows
+    if (kGated) bulk_prefetch_l2(p.gate + (size_t)colbase * p.rank, bytes);  // the candidates' gate rows
   }
   // gated head: this step's state, read while the chunk is recomputed
   float gs[8];
-  if (p.gate && stage_next && ew == 0 && 8 * lane < p.rank) gated_state_k(p, r, k, lane, gs);
+  if (kGated && stage_next && ew == 0 && 8 * lane < p.rank) gated_state_k(p, r, k, lane, gs);
   // bias of the 64 columns of chunk cstar: thread (row group rg, 8-column unit uc)
   float bcol = 0.f;
   if (et < kChunk && colbase + et < p.V)
@@ -537,11 +538,11 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
     const int tok = min(colbase + xc, p.V - 1);
     if (stage_next) {  // copy W1[tok] from the fetched chunk rows to the staging row
       uint4 zv = make_uint4(0, 0, 0, 0);
-      if (p.gate && 8 * lane < p.rank) zv = __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)tok * p.rank) + lane);
+      if (kGated && 8 * lane < p.rank) zv = __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)tok * p.rank) + lane);
       mbar_wait_drain(w1Full, w1_use & 1, p.status);
       if (8 * lane < p.rank) {
         const uint4 wv = *reinterpret_cast<const uint4*>(sBlk + (size_t)(tok - colbase) * p.rank * 2 + 16 * lane);
-        if (p.gate) {
+        if (kGated) {
           gated_update8(gs, zv, wv);
           store_gcarry(p, r, lane, gs);
           stage[lane] = pack_bf16x8(gs);
@@ -884,7 +885,7 @@ namespace dspark {
 // kResid = false: the gamma drafting steps. kResid = true: one pass of the
 // verifier's residual / bonus draw (A rows = W1[prev] of each request's
 // first rejected position, per-request target and base rows read directly).
-template <bool kResid, bool kLabel = false>
+template <bool kResid, bool kLabel = false, bool kGated = false>
 __global__ void __launch_bounds__(kPThreads, 1)
     persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                             const __grid_constant__ CUtensorMap mapA, PersistParams p) {
@@ -1071,7 +1072,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
           }
           const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)max(prev, 0) * p.rank);
-          if (p.gate) {  // gated head: s_1 = z[anchor] * W1[anchor] (exact), rounded to bf16
+          if (kGated) {  // gated head: s_1 = z[anchor] * W1[anchor] (exact), rounded to bf16
             const uint4* zsrc = reinterpret_cast<const uint4*>(p.gate + (size_t)max(prev, 0) * p.rank);
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
@@ -1249,7 +1250,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (kResid)
           locate_resid_row(p, r, sA, et);
         else
-          locate_row(p, r, k, sA, et, w1Full, w1_use);
+          locate_row<kGated>(p, r, k, sA, et, w1Full, w1_use);
         eg_sync();
       }
       if (!kResid) {
@@ -1291,11 +1292,14 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (!coop || sms <= 0) return cudaSuccess;
-  static std::atomic<unsigned long long> attr{0};
-  if (set_smem_limit_once((const void*)persistent_sweep_kernel<false>, (int)kPSmem, attr) != cudaSuccess)
+  static std::atomic<unsigned long long> attr{0}, attr_gated{0};
+  // the recurrent (gated) head is its own instantiation: the Markov kernel carries none of its code
+  const void* fn = a.gate ? (const void*)persistent_sweep_kernel<false, false, true>
+                          : (const void*)persistent_sweep_kernel<false>;
+  if (set_smem_limit_once(fn, (int)kPSmem, a.gate ? attr_gated : attr) != cudaSuccess)
     return cudaSuccess;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persistent_sweep_kernel<false>, kPThreads, kPSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kPThreads, kPSmem) !=
           cudaSuccess ||
       per_sm < 1)
     return cudaSuccess;
@@ -1347,7 +1351,7 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   void* args[] = {&mapW2, &mapBase, &mapA, &p};
-  e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<false>, dim3(p.n_cta), dim3(kPThreads), args,
+  e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
   return e;
