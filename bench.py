@@ -40,6 +40,14 @@ def peaks():
     return FALLBACK_HBM, "fallback"
 
 
+def bf16_peak_tflops():
+    """Dense bf16 peak for a kernel timed alone (the burst figure)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured bf16_tflops (burst)"
+    return 1900.0, "fallback"
+
+
 def algorithmic_bytes(cfg, L):
     """Bytes each pass must touch once (re-reads excluded)."""
     e = 2 if cfg.dtype == "bf16" else 4
@@ -313,6 +321,29 @@ def main():
     conf_cal = torch.empty_like(inp["conf"])
     t_sts_apply = time_stage(lambda: dspark.sts_apply(inp["conf"], t_sts, conf_cal), 5)
 
+    # the hidden-state path: base logits from the backbone's hidden states and the LM head
+    # (tensor cores), then the sequential draft on them; d = 7168 (DeepSeek hidden size)
+    hidden_path = None
+    if cfg.dtype == "bf16":
+        d_h = 7168
+        H = W.hidden_device(cfg, d_h, dev)
+        LMW = W.lm_head_device(cfg, d_h, dev)
+        base_h = torch.empty_like(inp["base"])
+        t_lm = time_stage(lambda: dspark.lm_head(H, LMW, base_h, ws), 5)
+        t_lm_draft = time_stage(lambda: (dspark.lm_head(H, LMW, base_h, ws),
+                                         dspark.draft_sequential(base_h, inp["anchor"], inp["W1"], inp["W2"], inp["T"],
+                                                                 inp["seed"], out.tokens, out.q_tok, out.q_stats, ws)), 3)
+        if dspark.device_status(ws) != dspark.OK:
+            raise RuntimeError("device status after the hidden-state path")
+        flops = 2.0 * R * gamma * d_h * V
+        bf16_peak, bf16_kind = bf16_peak_tflops()
+        hidden_path = {"d": d_h, "lm_head_us": t_lm * 1e3, "tflops": flops / (t_lm * 1e-3) / 1e12,
+                       "peak_tflops": bf16_peak, "peak_kind": bf16_kind,
+                       "frac": flops / (t_lm * 1e-3) / 1e12 / bf16_peak,
+                       "lm_head_plus_draft_us": t_lm_draft * 1e3,
+                       "h2d_bytes_hidden": H.numel() * 2, "h2d_bytes_base_logits": inp["base"].numel() * 2}
+        del H, LMW, base_h
+
     # the recurrent (gated) head: the same workload with a gate table [V, rank]
     gated = None
     if cfg.dtype == "bf16":
@@ -409,6 +440,7 @@ def main():
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
         "gated_head": gated,
+        "hidden_path": hidden_path,
         "labels": None if t_labels is None else {
             "us": t_labels * 1e3, "algorithmic_bytes": label_bytes(cfg),
             "achieved_gbs": label_bytes(cfg) / (t_labels * 1e-3) / 1e9,

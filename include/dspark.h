@@ -247,6 +247,25 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
                            dspark_stream_t stream);
 
 /*
+ * Base logits from the parallel backbone's hidden states (GeekNews page,
+ * "Etapa paralela": one backbone pass over the block gives hidden states and
+ * base logits; "Comunicação de estados ocultos": only the hidden state before
+ * the LM head has to travel, and the LM head runs where the logits are used).
+ *
+ *   hidden   [M, d] bf16      final hidden states (M = R * gamma block positions)
+ *   lm_head  [d, V] bf16      the (shared) LM head
+ *   logits   [M, V] bf16 out  bf16(hidden . lm_head): float32 accumulation on
+ *                             the tensor cores, one rounding to nearest (ties to
+ *                             even); [R, gamma, V] for dspark_draft_sequential
+ * Requirements: M >= 1, d >= 8 and d % 8 == 0, V >= 64 and V % 8 == 0, the
+ * three tensors 16-byte aligned. `workspace` (at least 256 bytes, 256-byte
+ * aligned; any DSpark workspace) receives the device status word.
+ */
+dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const void* hidden,
+                             const void* lm_head, void* logits, void* workspace,
+                             size_t workspace_bytes, dspark_stream_t stream);
+
+/*
  * Recurrent (gated) sequential head (GeekNews page, "Geração
  * semiautorregressiva": "Head RNN", the variant that keeps a recurrent state
  * of the whole prefix drafted in the block, updated through gates). The pages

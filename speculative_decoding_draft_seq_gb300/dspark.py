@@ -54,6 +54,8 @@ def _load():
     lib.dspark_round_gated.restype = i32
     lib.dspark_round_gated.argtypes = ([i32] * 5 + [vp] * 6 + [vp, vp, vp, i32, i32, f32, u64] +
                                        [vp] * 9 + [vp, sz, vp])
+    lib.dspark_lm_head.restype = i32
+    lib.dspark_lm_head.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.dspark_acceptance_labels.restype = i32
     lib.dspark_acceptance_labels.argtypes = [i32] * 5 + [vp] * 7 + [f32, vp, vp, sz, vp]
     lib.dspark_sts_scratch_bytes.restype = sz
@@ -138,6 +140,15 @@ def draft_sequential_gated(base, anchor, W1, gate, W2, temperature, seed, tokens
                                              _ptr(W1), _ptr(gate), _ptr(W2), float(temperature), int(seed),
                                              _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(ws), ws.numel(),
                                              _stream(stream)), "dspark_draft_sequential_gated")
+
+
+def lm_head(hidden, lm_head_w, logits, ws, stream=None):
+    """Base logits bf16(hidden . lm_head): hidden [..., d], lm_head [d, V],
+    logits [..., V] (bf16 tensors; the leading dimensions are flattened)."""
+    d, V = lm_head_w.shape
+    M = hidden.numel() // d
+    _check(lib.dspark_lm_head(M, d, V, _ptr(hidden), _ptr(lm_head_w), _ptr(logits), _ptr(ws), ws.numel(),
+                              _stream(stream)), "dspark_lm_head")
 
 
 def schedule(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, ws, stream=None):

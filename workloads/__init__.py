@@ -38,6 +38,7 @@ _MUL_B = 0x2C1B3C6D
 # Tensor stream salts.
 S_BASE, S_EXTRA, S_TARGET, S_W1, S_W2 = 0x1B873593, 0x5BD1E995, 0x27D4EB2F, 0x165667B1, 0x61C88647
 S_GATE = 0x3C6EF372
+S_HIDDEN, S_LMHEAD = 0x7A4E2B19, 0x1F83D9AB
 
 CAUSAL, LAGGED, ALL = 0, 1, 2
 
@@ -402,6 +403,41 @@ def weights_device(cfg, device):
     w1 = _finish_t(cfg, _noise_t(cfg, S_W1, idx, cfg.w_sd, table)).reshape(cfg.V, cfg.rank)
     w2 = _finish_t(cfg, _noise_t(cfg, S_W2, idx, cfg.w_sd, table)).reshape(cfg.rank, cfg.V)
     return w1.contiguous(), w2.contiguous()
+
+
+def hidden_np(cfg, d, rows):
+    """Final hidden states of block positions `rows` (flat r * gamma + k), [len(rows), d]
+    bf16 bits: N(0, 1)."""
+    rows = np.asarray(rows, dtype=np.uint64)
+    idx = rows[:, None] * np.uint64(d) + np.arange(d, dtype=np.uint64)[None, :]
+    return _bf16_bits_np(_noise_np(cfg, S_HIDDEN, idx, 1.0))
+
+
+def lm_head_np(cfg, d, cols=None):
+    """LM head [d, V] (or its columns `cols`) as bf16 bits: N(0, (1.5 / sqrt(d))^2), so
+    that the logits have the spread of the base logits."""
+    cols = np.arange(cfg.V, dtype=np.uint64) if cols is None else np.asarray(cols, dtype=np.uint64)
+    idx = np.arange(d, dtype=np.uint64)[:, None] * np.uint64(cfg.V) + cols[None, :]
+    return _bf16_bits_np(_noise_np(cfg, S_LMHEAD, idx, 1.5 / math.sqrt(d)))
+
+
+def hidden_device(cfg, d, device):
+    torch = _torch()
+    table = torch.from_numpy(norm_table()).to(device)
+    idx = torch.arange(cfg.R * cfg.gamma * d, dtype=torch.int64, device=device)
+    return _bf16_t(_noise_t(cfg, S_HIDDEN, idx, 1.0, table)).reshape(cfg.R, cfg.gamma, d).contiguous()
+
+
+def lm_head_device(cfg, d, device, rows_per_chunk=512):
+    torch = _torch()
+    table = torch.from_numpy(norm_table()).to(device)
+    out = torch.empty((d, cfg.V), dtype=torch.bfloat16, device=device)
+    for i0 in range(0, d, rows_per_chunk):
+        i1 = min(d, i0 + rows_per_chunk)
+        idx = (torch.arange(i0, i1, dtype=torch.int64, device=device)[:, None] * cfg.V +
+               torch.arange(cfg.V, dtype=torch.int64, device=device)[None, :])
+        out[i0:i1] = _bf16_t(_noise_t(cfg, S_LMHEAD, idx, 1.5 / math.sqrt(d), table))
+    return out
 
 
 def gate_device(cfg, device):
