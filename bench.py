@@ -190,9 +190,11 @@ def main():
     ap.add_argument("--cpu-requests", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
-    ap.add_argument("--profile", choices=["round", "draft"], default=None,
+    ap.add_argument("--profile", choices=["round", "draft", "gated", "lm_head"], default=None,
                     help="launch only, for an ncu capture: 'round' = one round then two verify calls, "
-                         "'draft' = three drafting calls; prints the device status")
+                         "'draft' = three drafting calls, 'gated' = three gated-head drafting calls, "
+                         "'lm_head' = three base-logit GEMMs at d = 7168 over 16,384 vocabulary columns; "
+                         "prints the device status")
     args = ap.parse_args()
 
     import workloads as W
@@ -250,10 +252,22 @@ def main():
                 dspark.verify(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], out.tokens,
                               out.q_tok, out.q_stats, out.sched_len, inp["T"], inp["seed"], out.out_tokens,
                               out.accepted_len, out.p_tok, ws)
-        else:
+        elif args.profile == "draft":
             for _ in range(3):
                 dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"],
                                         out.tokens, out.q_tok, out.q_stats, ws)
+        elif args.profile == "gated":
+            gate = W.gate_device(W.with_(cfg, gated=True), dev)
+            for _ in range(3):
+                dspark.draft_sequential_gated(inp["base"], inp["anchor"], inp["W1"], gate, inp["W2"], inp["T"],
+                                              inp["seed"], out.tokens, out.q_tok, out.q_stats, ws)
+        else:  # a slice of the vocabulary keeps the capture small (LM head 235 MB, larger than L2)
+            cfg_h = W.with_(cfg, V=16384)
+            H = W.hidden_device(cfg_h, 7168, dev)
+            LMW = W.lm_head_device(cfg_h, 7168, dev)
+            o = torch.empty((R, gamma, 16384), dtype=torch.bfloat16, device=dev)
+            for _ in range(3):
+                dspark.lm_head(H, LMW, o, ws)
         torch.cuda.synchronize()
         st = dspark.device_status(ws)
         print(json.dumps({"profile": args.profile, "workload": workload, "status": dspark.status_string(st)}))
