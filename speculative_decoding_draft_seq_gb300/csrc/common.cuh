@@ -18,6 +18,9 @@ constexpr int kChunk = 64;
 inline __host__ __device__ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline __host__ __device__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Pieces each target row is split into by the row-stats pass (one CTA each).
+constexpr int kVsSplit = 4;
+
 // Per-request pending draw of the verifier (residual or bonus).
 enum PendKind : int { kPendNone = 0, kPendResid = 1, kPendBonus = 2 };
 
@@ -30,7 +33,7 @@ struct WsLayout {
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
   size_t gcarry;   // float  [R][256]        gated head: float32 state of each request between steps
-  size_t vsplit;   // float4 [R][gamma+1][4] target row quarter stats (M_s, Z_s, max, argmax)
+  size_t vsplit;   // float4 [R][gamma+1][kVsSplit] target row piece stats (M_s, Z_s, max, argmax)
   size_t vcount;   // u32    [R*(gamma+1) + R] row / request completion counters (zero between calls)
   size_t lstage;   // bf16   [R*gamma][256]  acceptance labels: W1 rows of every (request, position)
   size_t lsum;     // u64    [R*gamma]       acceptance labels: 2^-40 sums of max(0, P - Q) (zero between calls)
@@ -55,7 +58,7 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
   L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
   L.gcarry = o;  o = align256(o + (size_t)R * 256 * sizeof(float));
-  L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * 4 * sizeof(float4));
+  L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * kVsSplit * sizeof(float4));
   L.lstage = o;  o = align256(o + (size_t)R * gamma * 256 * 2);
   L.lsum = o;    o = align256(o + (size_t)R * gamma * sizeof(unsigned long long));
   L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));

@@ -93,7 +93,6 @@ struct OnlineStat {
 // finds the first rejection, and the accepted tokens, the pending residual or
 // bonus draw, and the zeroed p of unscheduled positions are written.
 constexpr int kVsThreads = 256;
-constexpr int kVsSplit = 4;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
