@@ -188,6 +188,7 @@ def main():
     ap.add_argument("--config", default="ds")
     ap.add_argument("--temperature", type=float, default=None)
     ap.add_argument("--cpu-requests", type=int, default=48)
+    ap.add_argument("--no-graph", action="store_true", help="time direct dspark_round calls, no CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
     ap.add_argument("--profile", choices=["round", "draft", "gated", "lm_head"], default=None,
@@ -378,20 +379,47 @@ def main():
         except dspark.DSparkError:
             gated = None
 
+    # the round as a CUDA graph (its launches and memsets replayed as one unit, as a serving
+    # loop would run it); the direct call is timed beside it
+    graph, graph_note = None, None
+    if not args.no_graph:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                one_round()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                one_round()
+            graph.replay()
+            torch.cuda.synchronize()
+            if dspark.device_status(ws) != dspark.OK:
+                raise RuntimeError("device status after the graph replay")
+        except Exception as e:  # capture not possible here: time the direct call only
+            graph, graph_note = None, f"graph capture failed: {type(e).__name__}"
+            torch.cuda.synchronize()
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return ts
+
+    direct_ms = float(np.mean(timed(one_round, max(3, args.steps // 4)))) if graph is not None else None
     clocks = ClockSampler()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start(rank)
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        one_round()
-        b.record(stream)
-        b.synchronize()
-        times.append(a.elapsed_time(b))
+    times = timed(graph.replay if graph is not None else one_round, args.steps)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
@@ -449,7 +477,10 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "CUDA graph of one dspark_round call, replayed per step" if graph is not None
+                   else (graph_note or "direct dspark_round call per step")},
+        "round_us_direct_call": None if direct_ms is None else direct_ms * 1e3,
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},

@@ -1325,7 +1325,7 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
     const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
     if (!make_tmap_bf16(&mapA, ws_at<void>(a.ws, L.astage), 3, dims, strides, box)) return cudaSuccess;
   }
-  PersistParams p;
+  PersistParams p{};
   p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
   p.nc = ceil_div(a.V, kChunk);
   p.n_cta = p.nc < sms ? p.nc : sms;
