@@ -8,10 +8,15 @@
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles taken in M-fastest
 // order, so the CTAs working at one time read the same LM-head columns (one
-// DRAM read, the rest from L2) and the hidden states stay in L2.
+// DRAM read, the rest from L2) and the hidden states stay in L2. CTAs run in
+// pairs (a cluster of two) on the row tiles 2i and 2i + 1 of the same columns:
+// each loads half of the shared B tile and multicasts it to both, halving the
+// LM-head bytes the pair pulls from L2 per FLOP.
 //   warp 0      TMA producer of a 4-stage ring: A = 128 rows x 64 K of the
 //               hidden states (K-major, 128-byte swizzle), B = 64 K-rows x 256
-//               LM-head columns as four 64-column boxes (MN-major);
+//               LM-head columns as four 64-column boxes (MN-major; two from
+//               each CTA of the pair); a stage is refilled once both CTAs'
+//               MMAs have released it;
 //   warp 1      TMEM allocation and tcgen05.mma issue (kind::f16, M = 128,
 //               N = 256, K = 16) into two 256-column accumulators;
 //   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time, rounding to bf16,
@@ -38,12 +43,13 @@ constexpr uint32_t kHSmem = 1024 + kHStages * kHStage + 256;
 
 struct LmParams {
   int M, d, V;
-  int n_m, n_tiles, nk;
+  int n_m, n_n, nk;
   int a_rows;  // rows of one A box (min(M, 128))
   __nv_bfloat16* out;
   uint32_t* status;
 };
 
+template <bool kPair>
 __global__ void __launch_bounds__(kHThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapLM,
                    LmParams p) {
@@ -58,8 +64,16 @@ __global__ void __launch_bounds__(kHThreads, 1)
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // work items: (row tile, column tile), or (pair of row tiles, column tile) for a pair
+  const int crank = kPair ? (int)cluster_ctarank() : 0;
+  const int first = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int stride = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int n_rows = kPair ? ceil_div(p.n_m, 2) : p.n_m;
+  const int n_items = n_rows * p.n_n;
+  auto item_m = [&](int t) { return kPair ? 2 * (t % n_rows) + crank : t % n_rows; };
+  auto item_c0 = [&](int t) { return (t / n_rows) * 256; };
   if (tid == 0) {
-    for (int i = 0; i < kHStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < kHStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kPair ? 2 : 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kHEpiWarps); }
     mbar_init(drain, 1);
     *sAbort = 0;
@@ -71,6 +85,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // the peer's barriers exist before anything is multicast to them
   tc_fence_after();
   const uint32_t tmem = *sTmem;
 
@@ -82,17 +97,24 @@ __global__ void __launch_bounds__(kHThreads, 1)
       const uint64_t pol_w = l2_policy_evict_normal();  // re-read by the row tiles running alongside
       int n = 0;
       bool stop = false;
-      for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
-        const int m = t % p.n_m, c0 = (t / p.n_m) * 256;
+      for (int t = first; t < n_items && !stop; t += stride) {
+        const int m = item_m(t), c0 = item_c0(t);
         const int nbox = min(4, ceil_div(p.V - c0, 64));
         for (int kc = 0; kc < p.nk; ++kc, ++n) {
           const int stage = n % kHStages;
           if (!mbar_wait(&empty[stage], ((n / kHStages) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
           unsigned char* st = smem + stage * kHStage;
+          // the whole B tile lands here: this CTA's boxes and the peer's multicast ones
           mbar_expect_tx(&full[stage], (uint32_t)p.a_rows * 128 + (uint32_t)nbox * kHBBox);
           tma_load_2d(st, &mapH, kc * kHK, m * kHM, &full[stage], pol_h);
-          for (int j = 0; j < nbox; ++j)
-            tma_load_2d(st + kHABytes + j * kHBBox, &mapLM, c0 + 64 * j, kc * kHK, &full[stage], pol_w);
+          if (kPair) {
+            for (int j = 2 * crank; j < 2 * crank + 2 && j < nbox; ++j)
+              tma_load_2d_multicast(st + kHABytes + j * kHBBox, &mapLM, c0 + 64 * j, kc * kHK, &full[stage],
+                                    (uint16_t)0x3, pol_w);
+          } else {
+            for (int j = 0; j < nbox; ++j)
+              tma_load_2d(st + kHABytes + j * kHBBox, &mapLM, c0 + 64 * j, kc * kHK, &full[stage], pol_w);
+          }
         }
       }
       for (int i = 1; i <= kHStages && n - i >= 0; ++i)  // no copy outlives the CTA
@@ -102,8 +124,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
     if (lane == 0) {  // MMA issuer
       int n = 0, T = 0;
       bool stop = false;
-      for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x, ++T) {
-        const int c0 = (t / p.n_m) * 256;
+      for (int t = first; t < n_items && !stop; t += stride, ++T) {
+        const int c0 = item_c0(t);
         const int nbox = min(4, ceil_div(p.V - c0, 64));
         const int buf = T & 1;
         if (!mbar_wait(&accEmpty[buf], ((T >> 1) & 1) ^ 1, sAbort, p.status)) break;
@@ -121,7 +143,10 @@ __global__ void __launch_bounds__(kHThreads, 1)
             const uint64_t b_desc = smem_desc_sw128(smem_u32(st + kHABytes + kk * 2048), kHBBox, 1024);
             tc_mma_bf16(dt, a_desc, b_desc, idesc, (kc | kk) != 0);
           }
-          tc_commit(&empty[stage]);
+          if (kPair)
+            tc_commit_multicast(&empty[stage], (uint16_t)0x3);  // both CTAs' copies of the stage are free
+          else
+            tc_commit(&empty[stage]);
         }
         if (stop) break;
         tc_commit(&accFull[buf]);
@@ -132,8 +157,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
   } else {  // epilogue warps 2..5: warp w reads TMEM lanes 32 (w mod 4) ..
     const int q = warp & 3;
     int T = 0;
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++T) {
-      const int m = t % p.n_m, c0 = (t / p.n_m) * 256;
+    for (int t = first; t < n_items; t += stride, ++T) {
+      const int m = item_m(t), c0 = item_c0(t);
       const int ncol = min(256, p.V - c0);
       const int buf = T & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&accFull[buf], (T >> 1) & 1, sAbort, p.status))) break;
@@ -161,6 +186,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (kPair) cluster_sync();  // no arrival or copy from the peer is still on its way here
 }
 
 }  // namespace dspark
@@ -182,12 +208,14 @@ extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const v
   if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) return DSPARK_ERR_CUDA;
-  static std::atomic<unsigned long long> attr{0};
-  if (set_smem_limit_once((const void*)lm_head_kernel, (int)kHSmem, attr) != cudaSuccess) return DSPARK_ERR_CUDA;
+  static std::atomic<unsigned long long> attr{0}, attr_pair{0};
+  if (set_smem_limit_once((const void*)lm_head_kernel<false>, (int)kHSmem, attr) != cudaSuccess ||
+      set_smem_limit_once((const void*)lm_head_kernel<true>, (int)kHSmem, attr_pair) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   LmParams p;
   p.M = M; p.d = d; p.V = V;
   p.n_m = ceil_div(M, kHM);
-  p.n_tiles = p.n_m * ceil_div(V, 256);
+  p.n_n = ceil_div(V, 256);
   p.nk = ceil_div(d, kHK);
   p.a_rows = M < kHM ? M : kHM;
   p.out = static_cast<__nv_bfloat16*>(logits);
@@ -205,7 +233,34 @@ extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const v
     const uint32_t box[2] = {64, (uint32_t)kHK};
     if (!make_tmap_bf16(&mapLM, lm_head, 2, dims, strides, box)) return DSPARK_ERR_CUDA;
   }
-  const int grid = std::min(p.n_tiles, sms);
-  lm_head_kernel<<<grid, kHThreads, kHSmem, (cudaStream_t)stream>>>(mapH, mapLM, p);
+  cudaStream_t s = (cudaStream_t)stream;
+  // pairs of row tiles share their B tiles; a single row tile (M <= 128) runs unpaired
+  int clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kHThreads);
+  cfg.dynamicSmemBytes = kHSmem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (p.n_m > 1) {
+    cfg.gridDim = dim3(2 * sms / 2);
+    if (cudaOccupancyMaxActiveClusters(&clusters, lm_head_kernel<true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      clusters = 0;
+    }
+  }
+  if (clusters > 0) {
+    const int pairs = ceil_div(p.n_m, 2) * p.n_n;
+    cfg.gridDim = dim3(2 * std::min(clusters, pairs));
+    if (cudaLaunchKernelEx(&cfg, lm_head_kernel<true>, mapH, mapLM, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+  } else {
+    const int grid = std::min(p.n_m * p.n_n, sms);
+    lm_head_kernel<false><<<grid, kHThreads, kHSmem, s>>>(mapH, mapLM, p);
+  }
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
