@@ -35,6 +35,7 @@ constexpr int kHM = 128;                 // tile rows (MMA M)
 constexpr int kHK = 64;                  // K per stage
 constexpr int kHStages = 4;
 constexpr int kHEpiWarps = 4;
+constexpr int kHCluster = 2;             // CTAs sharing each B tile by multicast (2 or 4)
 constexpr int kHThreads = 32 * (2 + kHEpiWarps);
 constexpr uint32_t kHABytes = kHM * 128;            // 128 rows x 64 bf16
 constexpr uint32_t kHBBox = kHK * 128;              // 64 K-rows x 64 bf16 columns
@@ -49,7 +50,8 @@ struct LmParams {
   uint32_t* status;
 };
 
-template <bool kPair>
+// kC CTAs of a cluster work on kC row tiles of the same columns (kC = 1: no cluster).
+template <int kC>
 __global__ void __launch_bounds__(kHThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapLM,
                    LmParams p) {
@@ -65,15 +67,17 @@ __global__ void __launch_bounds__(kHThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // work items: (row tile, column tile), or (pair of row tiles, column tile) for a pair
+  constexpr bool kPair = kC > 1;
+  constexpr uint16_t kMask = (uint16_t)((1u << kC) - 1u);
   const int crank = kPair ? (int)cluster_ctarank() : 0;
-  const int first = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int stride = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int n_rows = kPair ? ceil_div(p.n_m, 2) : p.n_m;
+  const int first = (int)blockIdx.x / kC;
+  const int stride = (int)gridDim.x / kC;
+  const int n_rows = ceil_div(p.n_m, kC);
   const int n_items = n_rows * p.n_n;
-  auto item_m = [&](int t) { return kPair ? 2 * (t % n_rows) + crank : t % n_rows; };
+  auto item_m = [&](int t) { return kC * (t % n_rows) + crank; };
   auto item_c0 = [&](int t) { return (t / n_rows) * 256; };
   if (tid == 0) {
-    for (int i = 0; i < kHStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kPair ? 2 : 1); }
+    for (int i = 0; i < kHStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kC); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kHEpiWarps); }
     mbar_init(drain, 1);
     *sAbort = 0;
@@ -108,9 +112,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
           mbar_expect_tx(&full[stage], (uint32_t)p.a_rows * 128 + (uint32_t)nbox * kHBBox);
           tma_load_2d(st, &mapH, kc * kHK, m * kHM, &full[stage], pol_h);
           if (kPair) {
-            for (int j = 2 * crank; j < 2 * crank + 2 && j < nbox; ++j)
+            for (int j = crank * (4 / kC); j < (crank + 1) * (4 / kC) && j < nbox; ++j)
               tma_load_2d_multicast(st + kHABytes + j * kHBBox, &mapLM, c0 + 64 * j, kc * kHK, &full[stage],
-                                    (uint16_t)0x3, pol_w);
+                                    kMask, pol_w);
           } else {
             for (int j = 0; j < nbox; ++j)
               tma_load_2d(st + kHABytes + j * kHBBox, &mapLM, c0 + 64 * j, kc * kHK, &full[stage], pol_w);
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
             tc_mma_bf16(dt, a_desc, b_desc, idesc, (kc | kk) != 0);
           }
           if (kPair)
-            tc_commit_multicast(&empty[stage], (uint16_t)0x3);  // both CTAs' copies of the stage are free
+            tc_commit_multicast(&empty[stage], kMask);  // every CTA's copy of the stage is free
           else
             tc_commit(&empty[stage]);
         }
@@ -209,8 +213,8 @@ extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const v
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) return DSPARK_ERR_CUDA;
   static std::atomic<unsigned long long> attr{0}, attr_pair{0};
-  if (set_smem_limit_once((const void*)lm_head_kernel<false>, (int)kHSmem, attr) != cudaSuccess ||
-      set_smem_limit_once((const void*)lm_head_kernel<true>, (int)kHSmem, attr_pair) != cudaSuccess)
+  if (set_smem_limit_once((const void*)lm_head_kernel<1>, (int)kHSmem, attr) != cudaSuccess ||
+      set_smem_limit_once((const void*)lm_head_kernel<kHCluster>, (int)kHSmem, attr_pair) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   LmParams p;
   p.M = M; p.d = d; p.V = V;
@@ -239,7 +243,7 @@ extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const v
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.x = kHCluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kHThreads);
@@ -248,19 +252,19 @@ extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const v
   cfg.attrs = at;
   cfg.numAttrs = 1;
   if (p.n_m > 1) {
-    cfg.gridDim = dim3(2 * sms / 2);
-    if (cudaOccupancyMaxActiveClusters(&clusters, lm_head_kernel<true>, &cfg) != cudaSuccess) {
+    cfg.gridDim = dim3(kHCluster * (sms / kHCluster));
+    if (cudaOccupancyMaxActiveClusters(&clusters, lm_head_kernel<kHCluster>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       clusters = 0;
     }
   }
   if (clusters > 0) {
-    const int pairs = ceil_div(p.n_m, 2) * p.n_n;
-    cfg.gridDim = dim3(2 * std::min(clusters, pairs));
-    if (cudaLaunchKernelEx(&cfg, lm_head_kernel<true>, mapH, mapLM, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+    const int items = ceil_div(p.n_m, kHCluster) * p.n_n;
+    cfg.gridDim = dim3(kHCluster * std::min(clusters, items));
+    if (cudaLaunchKernelEx(&cfg, lm_head_kernel<kHCluster>, mapH, mapLM, p) != cudaSuccess) return DSPARK_ERR_CUDA;
   } else {
     const int grid = std::min(p.n_m * p.n_n, sms);
-    lm_head_kernel<false><<<grid, kHThreads, kHSmem, s>>>(mapH, mapLM, p);
+    lm_head_kernel<1><<<grid, kHThreads, kHSmem, s>>>(mapH, mapLM, p);
   }
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
