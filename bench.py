@@ -239,12 +239,20 @@ def main():
     __graft_entry__.build()
     from speculative_decoding_draft_seq_gb300 import dspark
 
-    inp = W.device_inputs(cfg, dev)
+    # each rank holds its own R requests (its own seed); with several ranks the scheduler ranks all
+    # ranks' requests against one table of world x the single-GPU size (see shard.py)
+    inp = W.device_inputs(W.with_(cfg, seed=cfg.seed + 101 * rank) if world > 1 else cfg, dev)
     R, gamma, V = cfg.R, cfg.gamma, cfg.V
     dt_code = dspark.BF16 if cfg.dtype == "bf16" else dspark.FP32
     ws = dspark.new_workspace(R, gamma, V, cfg.rank, dt_code, cfg.n_table, dev)
     out = dspark.RoundOutputs(R, gamma, dev)
     stream = torch.cuda.current_stream()
+    sharded = None
+    if world > 1:
+        from speculative_decoding_draft_seq_gb300.shard import ShardedRound
+        cfg_all = W.with_(cfg, R=cfg.R * world, n_table=cfg.n_table * world)
+        inp["sps"] = torch.from_numpy(W.sps_table(cfg_all)).to(dev)
+        sharded = ShardedRound(dspark, R, gamma, V, cfg.rank, dt_code, cfg_all.n_table, dev)
     if args.profile:
         if args.profile == "round":
             dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
@@ -278,6 +286,9 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def one_round():
+        if sharded is not None:  # draft, all-gather of confidences + global schedule, verify
+            sharded(inp, out)
+            return
         dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
                       inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
 
@@ -382,7 +393,7 @@ def main():
     # the round as a CUDA graph (its launches and memsets replayed as one unit, as a serving
     # loop would run it); the direct call is timed beside it
     graph, graph_note = None, None
-    if not args.no_graph:
+    if not args.no_graph and world == 1:
         try:
             side = torch.cuda.Stream()
             side.wait_stream(stream)
@@ -477,7 +488,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": (f"request-sharded x{world}: local draft and verify, all-gathered "
+                                   f"confidences, global schedule") if world > 1 else "single GPU",
                    "launch": "CUDA graph of one dspark_round call, replayed per step" if graph is not None
                    else (graph_note or "direct dspark_round call per step")},
         "round_us_direct_call": None if direct_ms is None else direct_ms * 1e3,
