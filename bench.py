@@ -14,9 +14,14 @@ pinned host memory and the results copied back inside the timed region.
 --impl reference times the oracle (the plain CPU implementation) on a bounded
 sample of the same workload on the host cores.
 
-Multi-GPU: the path shards by request with no exchange on the data path
-(replicas only): under torchrun every rank runs its own round on its own GPU,
-timing is the max over ranks and `value` sums all ranks' positions.
+One step at N = 1 replays the round captured as a CUDA graph (direct calls
+are timed beside it).
+
+Multi-GPU: the path shards by request. Under torchrun every rank drafts and
+verifies its own requests on its own GPU; the confidences are all-gathered
+(NCCL) and every rank runs the same global schedule over the whole batch
+(speculative_decoding_draft_seq_gb300/shard.py). Timing is the max over ranks
+and `value` sums all ranks' positions.
 """
 import argparse
 import json
