@@ -257,7 +257,7 @@ dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, in
  *   logits   [M, V] bf16 out  bf16(hidden . lm_head): float32 accumulation on
  *                             the tensor cores, one rounding to nearest (ties to
  *                             even); [R, gamma, V] for dspark_draft_sequential
- * Requirements: M >= 1, d >= 8 and d % 8 == 0, V >= 64 and V % 8 == 0, the
+ * Requirements: M >= 1, d >= 64 and d % 8 == 0, V >= 64 and V % 8 == 0, the
  * three tensors 16-byte aligned. `workspace` (at least 256 bytes, 256-byte
  * aligned; any DSpark workspace) receives the device status word.
  */

@@ -200,7 +200,8 @@ using namespace dspark;
 extern "C" dspark_status dspark_lm_head(int32_t M, int32_t d, int32_t V, const void* hidden, const void* lm_head,
                                         void* logits, void* workspace, size_t workspace_bytes,
                                         dspark_stream_t stream) {
-  if (M < 1 || d < 8 || d % 8 != 0 || V < 64 || V % 8 != 0 || (long long)M * V > (1ll << 40) || !hidden ||
+  // a TMA box is never wider than its tensor: d >= 64 (one K box) and V >= 64 (one column box)
+  if (M < 1 || d < 64 || d % 8 != 0 || V < 64 || V % 8 != 0 || (long long)M * V > (1ll << 40) || !hidden ||
       !lm_head || !logits)
     return DSPARK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(lm_head) |

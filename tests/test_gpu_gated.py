@@ -20,6 +20,7 @@ if torch.cuda.is_available():
 
 GATED = [
     # (R, gamma, V, rank): several chunks per CTA, a vocabulary tail, two M tiles
+    (1, 1, 64, 64),       # the smallest tensor-core shape: one request, one step, one chunk
     (33, 6, 640, 256),
     (150, 4, 3000, 64),
     (200, 3, 2056, 128),

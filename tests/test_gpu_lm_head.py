@@ -65,6 +65,8 @@ def _run(cfg, d, dev="cuda"):
 
 
 @pytest.mark.parametrize("M,d,V", [
+    (1, 64, 64),        # one row, one K step, one column box
+    (256, 64, 64),      # two row tiles (one CTA pair), one column box
     (200, 512, 1000),   # a partial row tile and a partial last column box
     (5, 64, 72),        # fewer rows than a tile, two column boxes
     (128, 136, 256),    # a K tail of 8
@@ -94,6 +96,17 @@ def test_lm_head_full_size_sampled():
     LM_bits = W.lm_head_np(cfg, d, cols)
     g = _bits(out).reshape(-1, cfg.V)[rows][:, cols]
     check_logits(g, H_bits, LM_bits)
+
+
+def test_lm_head_argument_errors():
+    dev = "cuda"
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    H = torch.zeros((4, 32), dtype=torch.bfloat16, device=dev)
+    LM = torch.zeros((32, 64), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((4, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(dspark.DSparkError) as e:  # d below one K box
+        dspark.lm_head(H, LM, out, ws)
+    assert e.value.status == dspark.ERR_INVALID_ARG
 
 
 def test_draft_from_hidden_states():
