@@ -350,6 +350,17 @@ dspark_status dspark_sts_apply(int32_t R, int32_t gamma, const float* conf, cons
  * (DSPARK_OK if no device-side error was recorded). */
 dspark_status dspark_device_status(const void* workspace, dspark_stream_t stream);
 
+/*
+ * Self-test of the bounded device waits: runs one wait of the kinds the
+ * kernels use on a condition nothing meets -- `which` 0 = the grid barrier,
+ * 1 = an mbarrier wait -- so that it gives up after its iteration limit
+ * (about a second), records DSPARK_ERR_TIMEOUT in the workspace's status word
+ * (read with dspark_device_status) and returns. Nothing traps; later calls on
+ * the same context work. Uses word 16 of the workspace's status block.
+ */
+dspark_status dspark_wait_selftest(int32_t which, void* workspace, size_t workspace_bytes,
+                                   dspark_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* dspark_status_string(dspark_status status);
 

@@ -45,7 +45,7 @@ constexpr uint32_t kPBBox = kPKC * 128;
 constexpr uint32_t kPBStage = 4 * kPBBox;
 constexpr uint32_t kPBaseBox = 128 * 128;
 constexpr uint32_t kPSmem = 1024 + kPABytes + kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox + 1024;
-constexpr uint32_t kGridSpinLimit = 1u << 22;
+constexpr uint32_t kGridSpinLimit = 1u << 20;  // about 1 s of polls
 
 // Scratch of the locate phase, carved from the A-operand region (free
 // between the last MMA of a step and the next gather).
@@ -1361,6 +1361,25 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
 
 namespace dspark {
 
+// Runs one of the kernels' bounded waits on a condition that nothing ever
+// meets, so that it gives up: `which` 0 = the grid barrier (a counter target
+// no launch reaches), 1 = an mbarrier phase that no arrival completes. The
+// wait records DSPARK_ERR_TIMEOUT in the status word and the kernel returns;
+// nothing traps and the context stays usable.
+__global__ void wait_selftest_kernel(int which, uint32_t* status, unsigned int* counter) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  if (which == 0) {
+    grid_barrier(counter, 0xFFFFFFFFu, status, &abort_flag);
+  } else {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    mbar_wait(&bar, 0, &abort_flag, status);  // phase 0 never completes: no arrival
+  }
+}
+
 bool gated_supported(const DraftArgs& a) {
   if (!a.gate || !draft_tc_eligible(a) || (reinterpret_cast<uintptr_t>(a.gate) & 15) != 0) return false;
   int dev = 0, coop = 0;
@@ -1512,3 +1531,17 @@ cudaError_t launch_label_persistent(const LabelArgs& a, cudaStream_t s, int& lau
 }
 
 }  // namespace dspark
+
+extern "C" dspark_status dspark_wait_selftest(int32_t which, void* workspace, size_t workspace_bytes,
+                                              dspark_stream_t stream) {
+  if (which != 0 && which != 1) return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 || workspace_bytes < 256)
+    return DSPARK_ERR_WORKSPACE;
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  // a counter of its own (word 16 of the status block), zeroed first: the target is never reached
+  unsigned int* counter = reinterpret_cast<unsigned int*>(status + 16);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  dspark::wait_selftest_kernel<<<1, 32, 0, s>>>(which, status, counter);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}

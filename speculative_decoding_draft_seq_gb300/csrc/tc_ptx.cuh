@@ -12,7 +12,7 @@ namespace dspark {
 
 // Iteration limit of every mbarrier wait loop: a wait that runs out records
 // DSPARK_ERR_TIMEOUT and the kernel winds down instead of spinning forever.
-constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 19;  // about 2 s of try_wait polls
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

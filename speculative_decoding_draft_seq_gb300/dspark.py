@@ -56,6 +56,8 @@ def _load():
                                        [vp] * 9 + [vp, sz, vp])
     lib.dspark_lm_head.restype = i32
     lib.dspark_lm_head.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.dspark_wait_selftest.restype = i32
+    lib.dspark_wait_selftest.argtypes = [i32, vp, sz, vp]
     lib.dspark_acceptance_labels.restype = i32
     lib.dspark_acceptance_labels.argtypes = [i32] * 5 + [vp] * 7 + [f32, vp, vp, sz, vp]
     lib.dspark_sts_scratch_bytes.restype = sz
@@ -243,6 +245,12 @@ def round_gated(base, target, anchor, W1, gate, W2, conf, conf_lagged, sps, mode
                                   _ptr(out.q_tok), _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K),
                                   _ptr(out.tau_theta), _ptr(out.out_tokens), _ptr(out.accepted_len),
                                   _ptr(out.p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_round_gated")
+
+
+def wait_selftest(which, ws, stream=None):
+    """A bounded device wait (0: grid barrier, 1: mbarrier) on a condition nothing meets; it
+    gives up and records ERR_TIMEOUT in the workspace's status word."""
+    _check(lib.dspark_wait_selftest(int(which), _ptr(ws), ws.numel(), _stream(stream)), "dspark_wait_selftest")
 
 
 def device_status(ws, stream=None):
