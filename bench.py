@@ -453,23 +453,42 @@ def main():
         host["conf_lag"] = inp["conf_lag"].cpu().pin_memory()
     # two slots of device inputs and outputs: while the round of step i runs on `stream`, the
     # inputs of step i + 1 are copied on a copy stream (as a serving loop would overlap them);
-    # every step's copies in and out are inside the timed region
+    # every step's copies in and out are inside the timed region. Of the target logits only the
+    # rows verification reads are sent (rows 0..L_r, dspark_copy_scheduled_rows): the step's
+    # confidences go first, the scheduler runs on them on its own workspace while the previous
+    # round computes, and its lengths come back to the host to pick the rows.
     res_keys = ("out_tokens", "accepted_len", "sched_len")
     outs = [out, dspark.RoundOutputs(R, gamma, dev)]
     res_host = [{k: torch.empty_like(getattr(o, k), device="cpu").pin_memory() for k in res_keys} for o in outs]
     dev_in = [{k: torch.empty_like(inp[k]) for k in host} for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in res_host[0].values())
-    copy_stream = torch.cuda.Stream()
+    small = sorted((k for k in host if k != "target"), key=lambda k: k != "conf" and k != "conf_lag")  # confidences first
+    ws_ahead = dspark.new_workspace(R, gamma, 1, cfg.rank, dt_code, cfg.n_table, dev)
+    L_dev = torch.empty(R, dtype=torch.int32, device=dev)
+    K_dev = torch.empty(1, dtype=torch.int32, device=dev)
+    tt_dev = torch.empty(2, dtype=torch.float64, device=dev)
+    L_host = torch.empty(R, dtype=torch.int32).pin_memory()
+    copy_stream, sched_stream = torch.cuda.Stream(), torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+    conf_in, L_back = torch.cuda.Event(), torch.cuda.Event()
+    sent = {"target": 0}
 
     def copy_in(j):
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(consumed[j])  # the round that last used slot j has read it
-            for k, v in host.items():
-                dev_in[j][k].copy_(v, non_blocking=True)
-            copied[j].record(copy_stream)
+            for k in small:
+                dev_in[j][k].copy_(host[k], non_blocking=True)
+            conf_in.record(copy_stream)
+        sched_stream.wait_event(conf_in)
+        dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev, K_dev,
+                        tt_dev, ws_ahead, stream=sched_stream)
+        with torch.cuda.stream(sched_stream):
+            L_host.copy_(L_dev, non_blocking=True)
+            L_back.record(sched_stream)
+        L_back.synchronize()  # the host picks the rows (the GPU keeps running the current round)
+        dspark.copy_scheduled_rows(host["target"], dev_in[j]["target"], L_host, stream=copy_stream)
+        sent["target"] = int((L_host.clamp(0, gamma) + 1).sum()) * V * host["target"].element_size()
+        copied[j].record(copy_stream)
 
     def compute(j):
         stream.wait_event(copied[j])
@@ -485,9 +504,9 @@ def main():
         a.record(copy_stream)
         copy_in(0)
         for i in range(n):
+            compute(i % 2)
             if i + 1 < n:
                 copy_in((i + 1) % 2)
-            compute(i % 2)
         b.record(stream)
         b.synchronize()
         return a.elapsed_time(b) / n
@@ -495,6 +514,8 @@ def main():
     e2e_run(2)
     torch.cuda.synchronize()
     e2e_ms = e2e_run(max(3, args.steps // 2))
+    h2d = sum(host[k].numel() * host[k].element_size() for k in small) + sent["target"]
+    d2h = sum(v.numel() * v.element_size() for v in res_host[0].values()) + L_host.numel() * 4
 
     L = out.sched_len.cpu().numpy()
     A = out.accepted_len.cpu().numpy()
@@ -535,7 +556,9 @@ def main():
                         "emitted_tokens_per_s": world * int((A + 1).sum()) / (ms * 1e-3)},
         "e2e": {"value": world * R * gamma / (e2e_ms * 1e-3), "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "overlap": "step i+1's host-to-device copies run during step i's round (two input slots)"},
+                "overlap": "step i+1's host-to-device copies run during step i's round (two input slots)",
+                "target_rows": "only rows 0..L_r of each request (those verification reads), picked by a "
+                               "look-ahead schedule of the step's confidences"},
         "clocks": clk,
         "gpu_launches": launches_per_round * args.steps,
     }

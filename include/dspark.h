@@ -351,6 +351,21 @@ dspark_status dspark_sts_apply(int32_t R, int32_t gamma, const float* conf, cons
 dspark_status dspark_device_status(const void* workspace, dspark_stream_t stream);
 
 /*
+ * Host-to-device copy of the target-logit rows verification reads: rows
+ * 0..sched_len[r] of every request r (dspark_verify reads no other row), one
+ * cudaMemcpyAsync per request on `stream`. host_target [R, gamma+1, V] dtype
+ * is HOST memory (pinned for the copies to be asynchronous), device_target
+ * the device tensor of the same shape (rows past sched_len[r] are left as
+ * they are), host_sched_len [R] int32 a HOST array (for instance the lengths
+ * of dspark_schedule copied back). For a serving loop that receives target
+ * logits from the host: the bytes sent follow the schedule, as the target's
+ * verification cost does.
+ */
+dspark_status dspark_copy_scheduled_rows(int32_t R, int32_t gamma, int32_t V, int32_t dtype,
+                                         const void* host_target, void* device_target,
+                                         const int32_t* host_sched_len, dspark_stream_t stream);
+
+/*
  * Self-test of the bounded device waits: runs one wait of the kinds the
  * kernels use on a condition nothing meets -- `which` 0 = the grid barrier,
  * 1 = an mbarrier wait -- so that it gives up after its iteration limit

@@ -300,6 +300,24 @@ dspark_status dspark_acceptance_labels(int32_t R, int32_t gamma, int32_t V, int3
   return cuda_status(e);
 }
 
+dspark_status dspark_copy_scheduled_rows(int32_t R, int32_t gamma, int32_t V, int32_t dtype, const void* host_target,
+                                        void* device_target, const int32_t* host_sched_len,
+                                        dspark_stream_t stream) {
+  if (R < 1 || gamma < 1 || V < 1 || (dtype != DSPARK_FP32 && dtype != DSPARK_BF16) || !host_target ||
+      !device_target || !host_sched_len)
+    return DSPARK_ERR_INVALID_ARG;
+  const size_t e = dtype == DSPARK_BF16 ? 2 : 4;
+  const size_t row = (size_t)V * e, req = (size_t)(gamma + 1) * row;
+  for (int r = 0; r < R; ++r) {
+    const int L = host_sched_len[r] < 0 ? 0 : (host_sched_len[r] > gamma ? gamma : host_sched_len[r]);
+    const size_t off = (size_t)r * req;
+    if (cudaMemcpyAsync(static_cast<char*>(device_target) + off, static_cast<const char*>(host_target) + off,
+                        (size_t)(L + 1) * row, cudaMemcpyHostToDevice, (cudaStream_t)stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  }
+  return DSPARK_OK;
+}
+
 dspark_status dspark_device_status(const void* workspace, dspark_stream_t stream) {
   if (!workspace) return DSPARK_ERR_WORKSPACE;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DSPARK_ERR_CUDA;

@@ -56,6 +56,8 @@ def _load():
                                        [vp] * 9 + [vp, sz, vp])
     lib.dspark_lm_head.restype = i32
     lib.dspark_lm_head.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.dspark_copy_scheduled_rows.restype = i32
+    lib.dspark_copy_scheduled_rows.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
     lib.dspark_wait_selftest.restype = i32
     lib.dspark_wait_selftest.argtypes = [i32, vp, sz, vp]
     lib.dspark_acceptance_labels.restype = i32
@@ -245,6 +247,14 @@ def round_gated(base, target, anchor, W1, gate, W2, conf, conf_lagged, sps, mode
                                   _ptr(out.q_tok), _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K),
                                   _ptr(out.tau_theta), _ptr(out.out_tokens), _ptr(out.accepted_len),
                                   _ptr(out.p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_round_gated")
+
+
+def copy_scheduled_rows(host_target, device_target, host_sched_len, stream=None):
+    """Host-to-device copy of target rows 0..L_r of every request (host_target pinned)."""
+    R, g1, V = host_target.shape
+    _check(lib.dspark_copy_scheduled_rows(R, g1 - 1, V, _dtype_code(host_target), _ptr(host_target),
+                                          _ptr(device_target), _ptr(host_sched_len), _stream(stream)),
+           "dspark_copy_scheduled_rows")
 
 
 def wait_selftest(which, ws, stream=None):
