@@ -161,14 +161,19 @@ def label_bytes(cfg):
     return (2 * cfg.R * cfg.gamma * cfg.V + cfg.rank * cfg.V + cfg.R * cfg.gamma * cfg.rank) * e
 
 
+# The sources the kernels with recorded DRAM traffic (the drafting sweep and its residual mode) are
+# compiled from: a change to any of them voids the record; host-only files (api.cu, the header's
+# declarations) do not.
+TRAFFIC_SOURCES = ("common.cuh", "draft_persistent.cu", "internal.h", "tc_ptx.cuh")
+
+
 def csrc_digest():
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_draft_seq_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(d, name), "rb").read())
+    for name in TRAFFIC_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(d, name), "rb").read())
     return h.hexdigest()
 
 
