@@ -237,3 +237,29 @@ def test_host_argument_errors_are_synchronous():
         dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
                       None, inp["sps"], W.CAUSAL, 1.0, 0, out, ws[:1024])
     assert e.value.status == dspark.ERR_WORKSPACE
+
+
+def test_copy_scheduled_rows_copies_exactly_the_verified_rows():
+    """dspark_copy_scheduled_rows: rows 0..L_r of each request arrive, every
+    other row of the device tensor is left as it was; a round on the device
+    tensor then equals the round on fully copied target logits."""
+    cfg = RAGGED_BF16
+    inp = device_inputs(cfg)
+    R, g1, V = inp["target"].shape
+    host = inp["target"].cpu().pin_memory()
+    L = torch.from_numpy(np.array([(3 * r) % (g1 + 2) - 1 for r in range(R)], dtype=np.int32))  # -1..gamma+1
+    dev = torch.full_like(inp["target"], 7.0)
+    dspark.copy_scheduled_rows(host, dev, L)
+    torch.cuda.synchronize()
+    got, ref = dev.cpu(), host
+    for r in range(R):
+        n = min(max(int(L[r]), 0), g1 - 1) + 1
+        assert torch.equal(got[r, :n], ref[r, :n])
+        assert torch.all(got[r, n:] == 7.0)
+    g_full = gpu_round(cfg, inp)
+    Ls = torch.from_numpy(g_full["sched_len"])
+    part = torch.full_like(inp["target"], 7.0)
+    dspark.copy_scheduled_rows(host, part, Ls)
+    g_part = gpu_round(cfg, dict(inp, target=part))
+    for key in ("out_tokens", "accepted_len", "p_tok", "sched_len"):
+        assert np.array_equal(g_full[key], g_part[key]), key
