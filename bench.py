@@ -378,7 +378,7 @@ def main():
                        "frac": flops / (t_lm * 1e-3) / 1e12 / bf16_peak,
                        "lm_head_plus_draft_us": t_lm_draft * 1e3,
                        "h2d_bytes_hidden": H.numel() * 2, "h2d_bytes_base_logits": inp["base"].numel() * 2}
-        del H, LMW, base_h
+        del base_h  # H and the LM head stay for the hidden-state end-to-end run below
 
     # the recurrent (gated) head: the same workload with a gate table [V, rank]
     gated = None
@@ -461,66 +461,86 @@ def main():
     # every step's copies in and out are inside the timed region. Of the target logits only the
     # rows verification reads are sent (rows 0..L_r, dspark_copy_scheduled_rows): the step's
     # confidences go first, the scheduler runs on them on its own workspace while the previous
-    # round computes, and its lengths come back to the host to pick the rows.
+    # round computes, and its lengths come back to the host to pick the rows. With `lm`, the
+    # step sends the backbone's hidden states instead of base logits and the base logits are
+    # computed on the device with the LM head (dspark_lm_head) before the round.
     res_keys = ("out_tokens", "accepted_len", "sched_len")
     outs = [out, dspark.RoundOutputs(R, gamma, dev)]
     res_host = [{k: torch.empty_like(getattr(o, k), device="cpu").pin_memory() for k in res_keys} for o in outs]
-    dev_in = [{k: torch.empty_like(inp[k]) for k in host} for _ in range(2)]
-    small = sorted((k for k in host if k != "target"), key=lambda k: k != "conf" and k != "conf_lag")  # confidences first
     ws_ahead = dspark.new_workspace(R, gamma, 1, cfg.rank, dt_code, cfg.n_table, dev)
     L_dev = torch.empty(R, dtype=torch.int32, device=dev)
     K_dev = torch.empty(1, dtype=torch.int32, device=dev)
     tt_dev = torch.empty(2, dtype=torch.float64, device=dev)
     L_host = torch.empty(R, dtype=torch.int32).pin_memory()
     copy_stream, sched_stream = torch.cuda.Stream(), torch.cuda.Stream()
-    copied = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
-    conf_in, L_back = torch.cuda.Event(), torch.cuda.Event()
-    sent = {"target": 0}
 
-    def copy_in(j):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(consumed[j])  # the round that last used slot j has read it
-            for k in small:
-                dev_in[j][k].copy_(host[k], non_blocking=True)
-            conf_in.record(copy_stream)
-        sched_stream.wait_event(conf_in)
-        dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev, K_dev,
-                        tt_dev, ws_ahead, stream=sched_stream)
-        with torch.cuda.stream(sched_stream):
-            L_host.copy_(L_dev, non_blocking=True)
-            L_back.record(sched_stream)
-        L_back.synchronize()  # the host picks the rows (the GPU keeps running the current round)
-        dspark.copy_scheduled_rows(host["target"], dev_in[j]["target"], L_host, stream=copy_stream)
-        sent["target"] = int((L_host.clamp(0, gamma) + 1).sum()) * V * host["target"].element_size()
-        copied[j].record(copy_stream)
+    def pipelined_e2e(host_in, n, lm=None):
+        small = sorted((k for k in host_in if k != "target"), key=lambda k: k != "conf" and k != "conf_lag")
+        dev_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host_in.items()} for _ in range(2)]
+        base_dev = [torch.empty_like(inp["base"]) for _ in range(2)] if lm is not None else None
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        conf_in, L_back = torch.cuda.Event(), torch.cuda.Event()
+        sent = {"target": 0}
 
-    def compute(j):
-        stream.wait_event(copied[j])
-        d = dev_in[j]
-        dspark.round_(d["base"], d["target"], d["anchor"], inp["W1"], inp["W2"], d["conf"], d.get("conf_lag"),
-                      inp["sps"], inp["mode"], inp["T"], inp["seed"], outs[j], ws)
-        consumed[j].record(stream)
-        for k, v in res_host[j].items():
-            v.copy_(getattr(outs[j], k), non_blocking=True)
+        def copy_in(j):
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[j])  # the round that last used slot j has read it
+                for k in small:
+                    dev_in[j][k].copy_(host_in[k], non_blocking=True)
+                conf_in.record(copy_stream)
+            sched_stream.wait_event(conf_in)
+            dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev, K_dev,
+                            tt_dev, ws_ahead, stream=sched_stream)
+            with torch.cuda.stream(sched_stream):
+                L_host.copy_(L_dev, non_blocking=True)
+                L_back.record(sched_stream)
+            L_back.synchronize()  # the host picks the rows (the GPU keeps running the current round)
+            dspark.copy_scheduled_rows(host_in["target"], dev_in[j]["target"], L_host, stream=copy_stream)
+            sent["target"] = int((L_host.clamp(0, gamma) + 1).sum()) * V * host_in["target"].element_size()
+            copied[j].record(copy_stream)
 
-    def e2e_run(n):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(copy_stream)
-        copy_in(0)
-        for i in range(n):
-            compute(i % 2)
-            if i + 1 < n:
-                copy_in((i + 1) % 2)
-        b.record(stream)
-        b.synchronize()
-        return a.elapsed_time(b) / n
+        def compute(j):
+            stream.wait_event(copied[j])
+            d = dev_in[j]
+            base = d["base"] if lm is None else base_dev[j]
+            if lm is not None:
+                dspark.lm_head(d["hidden"], lm, base, ws)
+            dspark.round_(base, d["target"], d["anchor"], inp["W1"], inp["W2"], d["conf"], d.get("conf_lag"),
+                          inp["sps"], inp["mode"], inp["T"], inp["seed"], outs[j], ws)
+            consumed[j].record(stream)
+            for k, v in res_host[j].items():
+                v.copy_(getattr(outs[j], k), non_blocking=True)
 
-    e2e_run(2)
-    torch.cuda.synchronize()
-    e2e_ms = e2e_run(max(3, args.steps // 2))
-    h2d = sum(host[k].numel() * host[k].element_size() for k in small) + sent["target"]
-    d2h = sum(v.numel() * v.element_size() for v in res_host[0].values()) + L_host.numel() * 4
+        def run(m):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(copy_stream)
+            copy_in(0)
+            for i in range(m):
+                compute(i % 2)
+                if i + 1 < m:
+                    copy_in((i + 1) % 2)
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) / m
+
+        run(2)
+        torch.cuda.synchronize()
+        ms_step = run(n)
+        h2d_b = sum(host_in[k].numel() * host_in[k].element_size() for k in small) + sent["target"]
+        d2h_b = sum(v.numel() * v.element_size() for v in res_host[0].values()) + L_host.numel() * 4
+        return ms_step, h2d_b, d2h_b
+
+    e2e_ms, h2d, d2h = pipelined_e2e(host, max(3, args.steps // 2))
+    if hidden_path is not None:  # the same loop sending hidden states (the LM head on the device)
+        host_h = {k: v for k, v in host.items() if k != "base"}
+        host_h["hidden"] = H.cpu().pin_memory()
+        h_ms, h_h2d, h_d2h = pipelined_e2e(host_h, max(3, args.steps // 8), lm=LMW)
+        if dspark.device_status(ws) != dspark.OK:
+            raise RuntimeError("device status after the hidden-state end-to-end run")
+        hidden_path["e2e"] = {"value": world * R * gamma / (h_ms * 1e-3), "unit": "positions/s",
+                              "h2d_bytes_per_step": h_h2d, "d2h_bytes_per_step": h_d2h, "ms_per_step": h_ms}
+        del H, LMW, host_h
 
     L = out.sched_len.cpu().numpy()
     A = out.accepted_len.cpu().numpy()
