@@ -89,10 +89,24 @@ def cpu_baseline(cfg, n_req, steps=1, warmup=0, timeout=900):
     dt = float(sum(ts))
     pos = n_req * cfg.gamma * len(ts)
     return {"value": pos / dt, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "host": {"nproc": os.cpu_count(), "cpu": host_cpu_model()},
             "sample": f"{len(ts)} step(s) of {n_req} of {cfg.R} requests x gamma={cfg.gamma} (drawn from the "
                       f"first {min(cfg.R, max(n_req, 8))}; each a full round: "
                       f"schedule over all requests, draft + verify of the sampled ones), single thread, "
                       f"{dt:.1f} s timed"}
+
+
+def host_cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo; Arm hosts report implementer and part)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in info:
+            if line.split(":")[0].strip() == key:
+                return line.split(":", 1)[1].strip()
+    return "unknown"
 
 
 class ClockSampler:
@@ -232,7 +246,7 @@ def main():
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": workload},
                 "cpu_baseline": {"value": v, "unit": "positions/s", "cores": 1, "kind": "oracle",
-                                 "sample": b["sample"]},
+                                 "sample": b["sample"], "host": b["host"]},
                 "e2e": {"value": v, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -441,6 +455,7 @@ def main():
     torch.cuda.synchronize()
     clocks.start(rank)
     times = timed(graph.replay if graph is not None else one_round, args.steps)
+    pct = {q: float(np.percentile(times, q)) * 1e3 for q in (10, 50, 90)}
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
@@ -561,6 +576,7 @@ def main():
                    "launch": "CUDA graph of one dspark_round call, replayed per step" if graph is not None
                    else (graph_note or "direct dspark_round call per step")},
         "round_us_direct_call": None if direct_ms is None else direct_ms * 1e3,
+        "round_us_p10_median_p90": [pct[10], pct[50], pct[90]],
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
