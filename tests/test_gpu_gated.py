@@ -92,3 +92,13 @@ def test_gated_refuses_shapes_off_the_tensor_core_path():
     with pytest.raises(dspark.DSparkError) as e:
         gpu_round(cfg, inp)
     assert e.value.status == dspark.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_gated_mixed_domain_sampled(T):
+    """The mixed-domain workload (256 requests: two M tiles, two CTAs' worth of
+    draws per step on some SMs) with the gated head, sampled and greedy."""
+    cfg = W.with_(W.CONFIGS["mixed"], T=T, gated=True)
+    requests = [0, 127, 128, 255]
+    g = gpu_round(cfg)
+    compare(cfg, g, oracle_round(cfg, requests), requests)

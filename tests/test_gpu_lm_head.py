@@ -144,3 +144,16 @@ def test_draft_from_hidden_states():
             assert abs(q[r, k] - o["q"][k]) <= 2e-3 * o["q"][k]
         compared += 1
     assert compared >= cfg.R // 2
+
+
+def test_lm_head_qwen_shape_sampled():
+    """A second model shape: Qwen3-4B's hidden size (2560) and vocabulary
+    (151,936, not a multiple of 256: a partial last column tile), a 7-token
+    block over 32 requests (two row tiles in one CTA pair)."""
+    cfg = W.Workload("lm_qwen", R=32, gamma=7, V=151936, rank=64, dtype="bf16", T=1.0, mode=W.CAUSAL, seed=6200)
+    d = 2560
+    H, LM, out = _run(cfg, d)
+    rows = np.array([0, 100, 127, 128, 223])
+    rng = np.random.default_rng(1)
+    cols = np.unique(np.concatenate([rng.choice(cfg.V, 2000, replace=False), np.arange(cfg.V - 300, cfg.V)]))
+    check_logits(_bits(out).reshape(-1, cfg.V)[rows][:, cols], W.hidden_np(cfg, d, rows), W.lm_head_np(cfg, d, cols))
