@@ -1166,64 +1166,70 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ++nh;
             const unsigned char* brow = sBase + s * kPBaseBox + row * 128;
             const int vbase = (c0 + j) * 64;
-            float m = -INFINITY, ssum = 0.f;
+            float m, ssum = 0.f;
             int am = 0x7fffffff;
             uint32_t accr[64];
             __syncwarp();
-            tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), accr);
+            // the accumulator load lands while the base logits are read from shared memory;
+            // both buffers are released as soon as their values are in registers
+            tmem_ld64_nowait(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), accr);
+            uint4 bx[8];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float acc[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(accr[half * 32 + i]);
-              float l[32];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int unit = half * 4 + u;
-                const uint4 x = *reinterpret_cast<const uint4*>(brow + ((unit ^ (row & 7)) << 4));
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  l[8 * u + 2 * e] = __fadd_rn(__uint_as_float(w[e] << 16), acc[8 * u + 2 * e]);
-                  l[8 * u + 2 * e + 1] = __fadd_rn(__uint_as_float(w[e] & 0xffff0000u), acc[8 * u + 2 * e + 1]);
-                }
-              }
-              const int vh = vbase + half * 32;
-              if (vh + 32 > p.V) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (vh + i >= p.V) l[i] = -INFINITY;
-              }
-              if (p.greedy) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (l[i] > m) { m = l[i]; am = vh + i; }
-              } else {
-                // four independent chains (the max is exact in any order;
-                // the sum is a float32 chunk partial either way)
-                float mq[4] = {l[0], l[1], l[2], l[3]};
-#pragma unroll
-                for (int i = 4; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], l[i]);
-                const float mn = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
-                const float mk = __fmul_rn(mn, kT);
-                float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sq[i & 3] += pweight(l[i], kT, mk);
-                const float sh = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-                ssum = (m == -INFINITY ? 0.f : ssum * pweight(m, kT, mk)) + sh;
-                m = mn;
-              }
-            }
+            for (int u = 0; u < 8; ++u) bx[u] = *reinterpret_cast<const uint4*>(brow + ((u ^ (row & 7)) << 4));
+            tmem_ld_wait();
             __syncwarp();
             if (lane == 0) mbar_arrive(&baseEmpty[s]);
+            if (j + 2 >= nbox) {  // this half's last chunk of the tile: the accumulator is free
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&accEmpty[buf]);
+            }
+            float l[64];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t w[4] = {bx[u].x, bx[u].y, bx[u].z, bx[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                l[8 * u + 2 * e] = __fadd_rn(__uint_as_float(w[e] << 16), __uint_as_float(accr[8 * u + 2 * e]));
+                l[8 * u + 2 * e + 1] =
+                    __fadd_rn(__uint_as_float(w[e] & 0xffff0000u), __uint_as_float(accr[8 * u + 2 * e + 1]));
+              }
+            }
+            if (vbase + 64 > p.V) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (vbase + i >= p.V) l[i] = -INFINITY;
+            }
+            if (p.greedy) {
+              m = -INFINITY;
+#pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (l[i] > m) { m = l[i]; am = vbase + i; }
+            } else {
+              // one pass: the chunk maximum (exact in any order), then the weights
+              // relative to it in eight independent chains (a float32 chunk partial)
+              float mq[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) mq[i] = l[i];
+#pragma unroll
+              for (int i = 8; i < 64; ++i) mq[i & 7] = fmaxf(mq[i & 7], l[i]);
+              m = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+              const float mk = __fmul_rn(m, kT);
+              float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int i = 0; i < 64; ++i) sq[i & 7] += pweight(l[i], kT, mk);
+              ssum = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
+            }
             const int r = mt * kPM + row;
             if (r < p.R)
               __stcg(p.part + (size_t)r * p.nc + (c0 + j),
                      p.greedy ? make_float2(m, __int_as_float(am)) : make_float2(m, ssum));
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accEmpty[buf]);
+          if (kResid || h >= nbox) {  // residual / label mode, or a half with no chunk in this tile
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accEmpty[buf]);
+          }
           if (stop) break;
         }
         if (kLabel && lacc) atomicAdd(p.lsum + pr, lacc);  // exact, order-free: deterministic
