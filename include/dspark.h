@@ -148,7 +148,7 @@ dspark_status dspark_schedule(int32_t R, int32_t gamma, const float* conf,
 
 /*
  * dspark_schedule without a workspace, for callers that cannot allocate device
- * memory. The paper has no counterpart to this entry point: it exists for
+ * memory. The pages describe no such entry point: it exists for
  * callers that run inside an engine which owns all device memory (a reserved
  * pool sized for weights and KV cache, with no allocator reachable from the
  * decode step), or that must not risk an allocation failing or fragmenting
