@@ -414,6 +414,30 @@ def main():
         except dspark.DSparkError:
             gated = None
 
+    # the full-verification bound: the same round with the scheduler in ALL mode, every drafted
+    # position verified (R * (gamma + 1) target rows), as the pages' offline evaluation runs it
+    full_verify = None
+    if world == 1:
+        fout = dspark.RoundOutputs(R, gamma, dev)
+        n_fv = max(3, args.steps // 8)
+        t_fround = time_stage(lambda: dspark.round_(
+            inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"], inp["conf_lag"],
+            inp["sps"], W.ALL, inp["T"], inp["seed"], fout, ws), n_fv)
+        t_fverify = time_stage(lambda: dspark.verify(
+            inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], fout.tokens, fout.q_tok,
+            fout.q_stats, fout.sched_len, inp["T"], inp["seed"], fout.out_tokens, fout.accepted_len, fout.p_tok,
+            ws), n_fv)
+        if dspark.device_status(ws) != dspark.OK:
+            raise RuntimeError("device status after the full-verification rounds")
+        Lf = fout.sched_len.cpu().numpy()
+        Af = fout.accepted_len.cpu().numpy()
+        bvf = algorithmic_bytes(cfg, Lf)[1]
+        full_verify = {"mode": "all", "round_us": t_fround * 1e3, "verify_us": t_fverify * 1e3,
+                       "verify_algorithmic_bytes": bvf,
+                       "verify_frac": bvf / (t_fverify * 1e-3) / 1e9 / peaks()[0],
+                       "scheduled_positions": int(Lf.sum()), "emitted": int((Af + 1).sum())}
+        del fout
+
     # the round as a CUDA graph (its launches and memsets replayed as one unit, as a serving
     # loop would run it); the direct call is timed beside it
     graph, graph_note = None, None
@@ -581,6 +605,7 @@ def main():
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
         "gated_head": gated,
+        "full_verify": full_verify,
         "hidden_path": hidden_path,
         "labels": None if t_labels is None else {
             "us": t_labels * 1e3, "algorithmic_bytes": label_bytes(cfg),
