@@ -514,7 +514,8 @@ def main():
     copy_stream, sched_stream = torch.cuda.Stream(), torch.cuda.Stream()
 
     def pipelined_e2e(host_in, n, lm=None):
-        small = sorted((k for k in host_in if k != "target"), key=lambda k: k != "conf" and k != "conf_lag")
+        small = [k for k in host_in if k != "target"]
+        conf_keys = [k for k in ("conf", "conf_lag") if k in host_in]
         dev_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host_in.items()} for _ in range(2)]
         base_dev = [torch.empty_like(inp["base"]) for _ in range(2)] if lm is not None else None
         copied = [torch.cuda.Event() for _ in range(2)]
@@ -525,9 +526,14 @@ def main():
         def copy_in(j):
             with torch.cuda.stream(copy_stream):
                 copy_stream.wait_event(consumed[j])  # the round that last used slot j has read it
-                for k in small:
+                # the confidences first: the look-ahead schedule and the host's choice of target rows
+                # then overlap the base-logit copy, and the row copies queue right behind it
+                for k in conf_keys:
                     dev_in[j][k].copy_(host_in[k], non_blocking=True)
                 conf_in.record(copy_stream)
+                for k in small:
+                    if k not in conf_keys:
+                        dev_in[j][k].copy_(host_in[k], non_blocking=True)
             sched_stream.wait_event(conf_in)
             dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev, K_dev,
                             tt_dev, ws_ahead, stream=sched_stream)
