@@ -31,7 +31,9 @@ def _conf(R, gamma, rng):
 
 
 CASES = [(40, 5, 260, "concave"), (128, 16, 2200, "step"), (256, 16, 4400, "cliff"),
-         (300, 20, 6400, "concave"), (1, 1, 4, "step"), (7, 3, 9, "cliff")]
+         (300, 20, 6400, "concave"), (1, 1, 4, "step"), (7, 3, 9, "cliff"),
+         # more than 8192 keys: the radix sort runs through the workspace (scheduler-stress size)
+         (1024, 16, 17408, "step"), (1024, 16, 16384, "cliff")]
 
 
 @pytest.mark.parametrize("R,gamma,n_table,table", CASES)
