@@ -490,6 +490,9 @@ def main():
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms = float(tt.item())
     value = world * R * gamma / (ms * 1e-3)
+    # the timed rounds' lengths (the end-to-end legs below write into `out` too)
+    L = out.sched_len.cpu().numpy()
+    A = out.accepted_len.cpu().numpy()
 
     # end to end through the same C ABI from pinned host buffers
     host = {k: inp[k].cpu().pin_memory() for k in ("base", "target", "anchor", "conf") }
@@ -587,8 +590,6 @@ def main():
                               "h2d_bytes_per_step": h_h2d, "d2h_bytes_per_step": h_d2h, "ms_per_step": h_ms}
         del H, LMW, host_h
 
-    L = out.sched_len.cpu().numpy()
-    A = out.accepted_len.cpu().numpy()
     peak, peak_kind = peaks()
     bd, bv = algorithmic_bytes(cfg, L)
     draft_gbs = bd / (t_draft * 1e-3) / 1e9
