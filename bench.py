@@ -537,13 +537,16 @@ def main():
                 for k in small:
                     if k not in conf_keys:
                         dev_in[j][k].copy_(host_in[k], non_blocking=True)
-            sched_stream.wait_event(conf_in)
-            dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev, K_dev,
-                            tt_dev, ws_ahead, stream=sched_stream)
-            with torch.cuda.stream(sched_stream):
-                L_host.copy_(L_dev, non_blocking=True)
-                L_back.record(sched_stream)
-            L_back.synchronize()  # the host picks the rows (the GPU keeps running the current round)
+            if sharded is None:
+                sched_stream.wait_event(conf_in)
+                dspark.schedule(dev_in[j]["conf"], dev_in[j].get("conf_lag"), inp["sps"], inp["mode"], L_dev,
+                                K_dev, tt_dev, ws_ahead, stream=sched_stream)
+                with torch.cuda.stream(sched_stream):
+                    L_host.copy_(L_dev, non_blocking=True)
+                    L_back.record(sched_stream)
+                L_back.synchronize()  # the host picks the rows (the GPU keeps running the current round)
+            else:  # the global schedule needs every rank's confidences: send every target row
+                L_host.fill_(gamma)
             dspark.copy_scheduled_rows(host_in["target"], dev_in[j]["target"], L_host, stream=copy_stream)
             sent["target"] = int((L_host.clamp(0, gamma) + 1).sum()) * V * host_in["target"].element_size()
             copied[j].record(copy_stream)
@@ -554,8 +557,12 @@ def main():
             base = d["base"] if lm is None else base_dev[j]
             if lm is not None:
                 dspark.lm_head(d["hidden"], lm, base, ws)
-            dspark.round_(base, d["target"], d["anchor"], inp["W1"], inp["W2"], d["conf"], d.get("conf_lag"),
-                          inp["sps"], inp["mode"], inp["T"], inp["seed"], outs[j], ws)
+            if sharded is not None:  # local draft and verify, all-gathered confidences, global schedule
+                sharded(dict(inp, base=base, target=d["target"], anchor=d["anchor"], conf=d["conf"],
+                             conf_lag=d.get("conf_lag")), outs[j])
+            else:
+                dspark.round_(base, d["target"], d["anchor"], inp["W1"], inp["W2"], d["conf"], d.get("conf_lag"),
+                              inp["sps"], inp["mode"], inp["T"], inp["seed"], outs[j], ws)
             consumed[j].record(stream)
             for k, v in res_host[j].items():
                 v.copy_(getattr(outs[j], k), non_blocking=True)
