@@ -95,6 +95,7 @@ struct PersistParams {
   int n_pairs;                  // R * gamma
   unsigned long long* lsum;     // [R * gamma] 2^-40 sums of max(0, P - Q), zero between calls
   float* labels;                // [R, gamma]
+  int label_tma;                // label pass: target and base boxes by TMA (else per-warp row copies)
 };
 
 // Per-request constants of the residual pass: P(v) = 2^((t_v - M_P) log2e/T) / Z_P
@@ -636,6 +637,17 @@ static_assert(2 * kPBStage + kPEpiWarps * kRsWarpBytes <= kPBStages * kPBStage +
               "the residual layout (2 W2 stages + row staging) fits where the drafting layout keeps 3 stages "
               "and the base ring");
 
+// Label pass with TMA rows: the 128 pairs of an M tile are consecutive flat
+// (request, position) indices, so a chunk's base rows are one box of the
+// base logits viewed as [R * gamma][V], and its target rows one box of the
+// target logits [R][gamma + 1][V] taking gamma positions of 128 / gamma
+// requests. Three slots of (target box, base box) in the staging region,
+// filled by warp 2 in chunk order and released by the four warps of the
+// epilogue half that reads them.
+constexpr int kLSlots = 3;
+constexpr uint32_t kLSlotBytes = 2 * kPBaseBox;
+static_assert(kLSlots * kLSlotBytes <= kPEpiWarps * kRsWarpBytes, "the label slots fit the staging region");
+
 struct ResidCopyRows {  // per lane: global rows of the four (copy, row) slots it serves
   int trow[4], brow[4];   // -1: zero fill
 };
@@ -709,6 +721,35 @@ __device__ __forceinline__ void resid_half(const PersistParams& p, const ResidRo
       const bool in = col < nvalid;
       sw[u] += in ? fmaxf(0.f, __fsub_rn(P, Q)) : 0.f;
       sp[u] += in ? P : 0.f;
+    }
+  }
+}
+
+// The same weights for the label pass when its rows arrive by TMA: one slot
+// holds a chunk's target box (128 pairs x 64 columns, 128-byte swizzle: the
+// 16-byte unit u of row m at m * 128 + ((u ^ (m & 7)) << 4)) followed by its
+// base box in the same layout; half hh is units 4 hh .. 4 hh + 3.
+__device__ __forceinline__ void label_half_tma(const PersistParams& p, const ResidRow& rr, int v0, uint32_t taddr,
+                                               const unsigned char* slot, int m, int hh, float (&sw)[4]) {
+  float acc[32];
+  __syncwarp();
+  tmem_ld32(taddr, acc);
+  if (rr.kind == kPendNone) return;
+  const float kT = p.kT, MPk = rr.MPk, invZP = rr.invZP, MQk = rr.MQk, invZQ = rr.invZQ;
+  const int nvalid = p.V - v0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t off = (uint32_t)(m * 128 + (((4 * hh + u) ^ (m & 7)) << 4));
+    const uint4 tv = *reinterpret_cast<const uint4*>(slot + off);
+    const uint4 bv = *reinterpret_cast<const uint4*>(slot + kPBaseBox + off);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int col = 8 * u + e;
+      const float t = unpack_bf16(tv, e);
+      const float l = __fadd_rn(unpack_bf16(bv, e), acc[col]);
+      const float P = __fmul_rn(pweight(t, kT, MPk), invZP);
+      const float Q = __fmul_rn(pweight(l, kT, MQk), invZQ);
+      sw[u] += col < nvalid ? fmaxf(0.f, __fsub_rn(P, Q)) : 0.f;
     }
   }
 }
@@ -888,7 +929,8 @@ namespace dspark {
 template <bool kResid, bool kLabel = false, bool kGated = false>
 __global__ void __launch_bounds__(kPThreads, 1)
     persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
-                            const __grid_constant__ CUtensorMap mapA, PersistParams p) {
+                            const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapT,
+                            PersistParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // drafting: A | 3 W2 stages | base ring; residual pass: A | 2 W2 stages |
@@ -983,6 +1025,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int n = nh[h] - i;
           mbar_wait_drain(&baseFull[h * kPBaseStages + n % kPBaseStages], (n / kPBaseStages) & 1, p.status);
         }
+    } else if (kLabel && p.label_tma && lane == 0) {  // label pass: target and base boxes, chunk order
+      prefetch_tensormap(&mapBase);
+      prefetch_tensormap(&mapT);
+      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t bytes = (uint32_t)p.box_rows * 128;
+      const int per_req = p.box_rows / p.gamma;  // requests per M tile of pairs
+      int n = 0;
+      bool stop = false;
+      for (int mt = 0; mt < p.n_mt && !stop; ++mt)
+        for (int t = 0; t < n_tiles && !stop; ++t) {
+          const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
+          for (int j = 0; j < nbox; ++j, ++n) {
+            const int slot = n % kLSlots;
+            if (!mbar_wait(&baseEmpty[slot], ((n / kLSlots) & 1) ^ 1, sAbort, p.status)) { stop = true; break; }
+            mbar_expect_tx(&baseFull[slot], 2 * bytes);
+            unsigned char* dst = sBase + (size_t)slot * kLSlotBytes;
+            tma_load_3d(dst, &mapT, (c0 + j) * 64, 0, mt * per_req, &baseFull[slot], pol);
+            tma_load_3d(dst + kPBaseBox, &mapBase, (c0 + j) * 64, mt * kPM, 0, &baseFull[slot], pol);
+          }
+        }
+      for (int i = 1; i <= kLSlots && n - i >= 0; ++i)
+        mbar_wait_drain(&baseFull[(n - i) % kLSlots], ((n - i) / kLSlots) & 1, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
@@ -1030,6 +1094,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else {
     // epilogue warps 3..10: A gather, softmax partials, grid barriers, locate
     const int et = tid - 96, ew = et >> 5;
+    const bool ltma = kLabel && p.label_tma;  // label pass fed by TMA boxes (warp 2)
     const int q = warp & 3, h = (warp - 3) >> 2;
     const int row = 32 * q + lane;
     const float kT = p.kT;
@@ -1126,9 +1191,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (kResid) {
           __syncwarp();  // the previous M tile's reads of the buffers are done
           rr = kLabel ? load_label_row(p, pr) : load_resid_row(p, pr);
-          cr = resid_copy_rows(p, rr, kLabel ? pr / p.gamma : pr, lane);
-          resid_issue(p, cr, hc_col(0), lane, rs_base);
-          resid_issue(p, cr, hc_col(1), lane, rs_base + kRsBufBytes);
+          if (!ltma) {
+            cr = resid_copy_rows(p, rr, kLabel ? pr / p.gamma : pr, lane);
+            resid_issue(p, cr, hc_col(0), lane, rs_base);
+            resid_issue(p, cr, hc_col(1), lane, rs_base + kRsBufBytes);
+          }
         }
         for (int t = 0; t < n_tiles; ++t, ++T) {
           const int buf = T & 1;
@@ -1140,15 +1207,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (kResid) {
               const int r = mt * kPM + row;
               float sw[4] = {0.f, 0.f, 0.f, 0.f}, sp[4] = {0.f, 0.f, 0.f, 0.f};
+              if (ltma) {  // this chunk's slot: chunk number n of the CTA's chunk sequence
+                const int n = mt * (c_end - c_begin) + 4 * t + j, slot = n % kLSlots;
+                if (!__all_sync(0xffffffffu, mbar_wait(&baseFull[slot], (n / kLSlots) & 1, sAbort, p.status))) {
+                  stop = true;
+                  break;
+                }
+                const unsigned char* sl = sBase + (size_t)slot * kLSlotBytes;
 #pragma unroll 1
-              for (int hh = 0; hh < 2; ++hh, ++hs) {
-                __syncwarp();  // every lane is done with the buffer the next copies overwrite
-                resid_issue(p, cr, hc_col(hs + 2), lane, rs_base + (uint32_t)((hs + 2) % kRsBufs) * kRsBufBytes);
-                asm volatile("cp.async.wait_group 2;" ::: "memory");
+                for (int hh = 0; hh < 2; ++hh)
+                  label_half_tma(p, rr, (c0 + j) * 64 + 32 * hh,
+                                 tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh), sl,
+                                 row, hh, sw);
                 __syncwarp();
-                resid_half(p, rr, (c0 + j) * 64 + 32 * hh,
-                           tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh),
-                           sBase + (size_t)ew * kRsWarpBytes + (size_t)(hs % kRsBufs) * kRsBufBytes, lane, sw, sp);
+                if (lane == 0) mbar_arrive(&baseEmpty[slot]);
+              } else {
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh, ++hs) {
+                  __syncwarp();  // every lane is done with the buffer the next copies overwrite
+                  resid_issue(p, cr, hc_col(hs + 2), lane, rs_base + (uint32_t)((hs + 2) % kRsBufs) * kRsBufBytes);
+                  asm volatile("cp.async.wait_group 2;" ::: "memory");
+                  __syncwarp();
+                  resid_half(p, rr, (c0 + j) * 64 + 32 * hh,
+                             tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh),
+                             sBase + (size_t)ew * kRsWarpBytes + (size_t)(hs % kRsBufs) * kRsBufBytes, lane, sw, sp);
+                }
               }
               if (kLabel) {
                 if (rr.kind != kPendNone) lacc += fx40((sw[0] + sw[1]) + (sw[2] + sw[3]));
@@ -1356,7 +1439,7 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapBase, &mapA, &p};
+  void* args[] = {&mapW2, &mapBase, &mapA, &mapW2, &p};  // no target map in this mode
   e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
@@ -1456,7 +1539,7 @@ cudaError_t launch_resid_persistent(const VerifyArgs& a, cudaStream_t s, int& la
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapW2, &mapA, &p};  // no base map in residual mode
+  void* args[] = {&mapW2, &mapW2, &mapA, &mapW2, &p};  // no base or target map in residual mode
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true>, dim3(p.n_cta), dim3(kPThreads), args,
                                   kPSmem, s);
   launches += 1;
@@ -1526,10 +1609,26 @@ cudaError_t launch_label_persistent(const LabelArgs& a, cudaStream_t s, int& lau
   p.n_pairs = n_pairs;
   p.lsum = ws_at<unsigned long long>(a.ws, L.lsum);
   p.labels = a.labels;
+  // rows by TMA when a tile's pairs are whole requests' position ranges (gamma divides the tile's rows)
+  CUtensorMap mapBL = mapW2, mapT = mapW2;
+  bool ltma = p.box_rows % a.gamma == 0 && (reinterpret_cast<uintptr_t>(a.base) & 15) == 0;
+  if (ltma) {  // base logits as [R * gamma][V] in pair order; a box = 64 columns of box_rows pairs
+    const uint64_t dims[3] = {(uint64_t)a.V, (uint64_t)n_pairs, 1};
+    const uint64_t strides[2] = {(uint64_t)a.V * 2, (uint64_t)n_pairs * a.V * 2};
+    const uint32_t box[3] = {64, (uint32_t)p.box_rows, 1};
+    ltma = make_tmap_bf16(&mapBL, a.base, 3, dims, strides, box);
+  }
+  if (ltma) {  // target rows 0..gamma-1 of each request; a box = 64 columns x gamma rows x box_rows/gamma requests
+    const uint64_t dims[3] = {(uint64_t)a.V, (uint64_t)a.gamma, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)a.V * 2, (uint64_t)(a.gamma + 1) * a.V * 2};
+    const uint32_t box[3] = {64, (uint32_t)a.gamma, (uint32_t)(p.box_rows / a.gamma)};
+    ltma = make_tmap_bf16(&mapT, a.target, 3, dims, strides, box);
+  }
+  p.label_tma = ltma ? 1 : 0;
   taken = true;
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
-  void* args[] = {&mapW2, &mapW2, &mapA, &p};  // no base map in this mode
+  void* args[] = {&mapW2, &mapBL, &mapA, &mapT, &p};
   e = cudaLaunchCooperativeKernel((const void*)persistent_sweep_kernel<true, true>, dim3(p.n_cta), dim3(kPThreads),
                                   args, kPSmem, s);
   launches += 1;
