@@ -42,7 +42,11 @@ SHAPES = [W.Workload("lab_tc", R=150, gamma=4, V=3000, rank=64, dtype="bf16", T=
                      n_table=750),
           W.Workload("lab_small", R=9, gamma=7, V=2056, rank=256, dtype="bf16", T=0.7, mode=W.CAUSAL, seed=5002,
                      base_sd=1.5, w_sd=0.05, target_sd=(1.0,), conf_law="decreasing", table="concave",
-                     n_table=72)]
+                     n_table=72),
+          # gamma = 6 does not divide the 128-pair tile: the rows are copied per warp, not by TMA boxes
+          W.Workload("lab_rows", R=40, gamma=6, V=1000, rank=128, dtype="bf16", T=1.0, mode=W.CAUSAL, seed=5003,
+                     base_sd=1.5, w_sd=0.05, target_sd=(0.6,), conf_law="decreasing", table="concave",
+                     n_table=280)]
 
 
 @pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
