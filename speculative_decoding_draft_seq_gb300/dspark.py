@@ -90,8 +90,22 @@ def last_launch_count():
     return int(lib.dspark_last_launch_count())
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+_I32, _F32, _F64, _U8 = torch.int32, torch.float32, torch.float64, torch.uint8
+
+
+def _ptr(t, dtype=None, host=False):
+    """Data pointer of a dense tensor for the C ABI, which takes row-major arrays without strides:
+    a non-contiguous view, a tensor on the wrong side of the host/device split or (where the entry
+    point fixes it) the wrong element type is refused here rather than read or written wrongly."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous (the C ABI takes dense row-major arrays)")
+    if t.is_cuda == host:
+        raise ValueError("expected a host tensor" if host else "expected a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -122,17 +136,17 @@ def new_workspace(R, gamma, V, rank, dtype, n_table, device="cuda", stream=None)
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     ws = ws[off:off + n]
-    _check(lib.dspark_workspace_init(_ptr(ws), n, _stream(stream)), "dspark_workspace_init")
+    _check(lib.dspark_workspace_init(_ptr(ws, _U8), n, _stream(stream)), "dspark_workspace_init")
     return ws
 
 
 def draft_sequential(base, anchor, W1, W2, temperature, seed, tokens, q_tok, q_stats, ws, stream=None):
     R, gamma, V = base.shape
     rank = W1.shape[1]
-    _check(lib.dspark_draft_sequential(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor),
-                                       _ptr(W1), _ptr(W2), float(temperature), int(seed), _ptr(tokens),
-                                       _ptr(q_tok), _ptr(q_stats), _ptr(ws), ws.numel(), _stream(stream)),
-           "dspark_draft_sequential")
+    _check(lib.dspark_draft_sequential(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor, _I32),
+                                       _ptr(W1), _ptr(W2), float(temperature), int(seed), _ptr(tokens, _I32),
+                                       _ptr(q_tok, _F32), _ptr(q_stats, _F32), _ptr(ws, _U8), ws.numel(),
+                                       _stream(stream)), "dspark_draft_sequential")
 
 
 def draft_sequential_gated(base, anchor, W1, gate, W2, temperature, seed, tokens, q_tok, q_stats, ws,
@@ -140,10 +154,11 @@ def draft_sequential_gated(base, anchor, W1, gate, W2, temperature, seed, tokens
     """Drafting with the recurrent (gated) head; `gate` [V, rank] like W1."""
     R, gamma, V = base.shape
     rank = W1.shape[1]
-    _check(lib.dspark_draft_sequential_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor),
+    _check(lib.dspark_draft_sequential_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(anchor, _I32),
                                              _ptr(W1), _ptr(gate), _ptr(W2), float(temperature), int(seed),
-                                             _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(ws), ws.numel(),
-                                             _stream(stream)), "dspark_draft_sequential_gated")
+                                             _ptr(tokens, _I32), _ptr(q_tok, _F32), _ptr(q_stats, _F32),
+                                             _ptr(ws, _U8), ws.numel(), _stream(stream)),
+           "dspark_draft_sequential_gated")
 
 
 def lm_head(hidden, lm_head_w, logits, ws, stream=None):
@@ -151,15 +166,15 @@ def lm_head(hidden, lm_head_w, logits, ws, stream=None):
     logits [..., V] (bf16 tensors; the leading dimensions are flattened)."""
     d, V = lm_head_w.shape
     M = hidden.numel() // d
-    _check(lib.dspark_lm_head(M, d, V, _ptr(hidden), _ptr(lm_head_w), _ptr(logits), _ptr(ws), ws.numel(),
+    _check(lib.dspark_lm_head(M, d, V, _ptr(hidden), _ptr(lm_head_w), _ptr(logits), _ptr(ws, _U8), ws.numel(),
                               _stream(stream)), "dspark_lm_head")
 
 
 def schedule(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, ws, stream=None):
     R, gamma = conf.shape
-    _check(lib.dspark_schedule(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(), int(mode),
-                               _ptr(sched_len), _ptr(K), _ptr(tau_theta), _ptr(ws), ws.numel(),
-                               _stream(stream)), "dspark_schedule")
+    _check(lib.dspark_schedule(R, gamma, _ptr(conf, _F32), _ptr(conf_lagged, _F32), _ptr(sps, _F32), sps.numel(),
+                               int(mode), _ptr(sched_len, _I32), _ptr(K, _I32), _ptr(tau_theta, _F64),
+                               _ptr(ws, _U8), ws.numel(), _stream(stream)), "dspark_schedule")
 
 
 def schedule_static(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, device_status=None,
@@ -167,19 +182,20 @@ def schedule_static(conf, conf_lagged, sps, mode, sched_len, K, tau_theta, devic
     """dspark_schedule_static: the scheduler without a workspace (fixed library
     scratch, R * gamma <= 16384). Returns the C status code without raising."""
     R, gamma = conf.shape
-    return int(lib.dspark_schedule_static(R, gamma, _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(),
-                                          int(mode), _ptr(sched_len), _ptr(K), _ptr(tau_theta),
-                                          _ptr(device_status), _stream(stream)))
+    return int(lib.dspark_schedule_static(R, gamma, _ptr(conf, _F32), _ptr(conf_lagged, _F32), _ptr(sps, _F32),
+                                          sps.numel(), int(mode), _ptr(sched_len, _I32), _ptr(K, _I32),
+                                          _ptr(tau_theta, _F64), _ptr(device_status), _stream(stream)))
 
 
 def verify(target, base, anchor, W1, W2, tokens, q_tok, q_stats, sched_len, temperature, seed,
            out_tokens, accepted_len, p_tok, ws, stream=None):
     R, gamma, V = base.shape
     rank = W1.shape[1]
-    _check(lib.dspark_verify(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base), _ptr(anchor),
-                             _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_tok), _ptr(q_stats), _ptr(sched_len),
-                             float(temperature), int(seed), _ptr(out_tokens), _ptr(accepted_len),
-                             _ptr(p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_verify")
+    _check(lib.dspark_verify(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base), _ptr(anchor, _I32),
+                             _ptr(W1), _ptr(W2), _ptr(tokens, _I32), _ptr(q_tok, _F32), _ptr(q_stats, _F32),
+                             _ptr(sched_len, _I32), float(temperature), int(seed), _ptr(out_tokens, _I32),
+                             _ptr(accepted_len, _I32), _ptr(p_tok, _F32), _ptr(ws, _U8), ws.numel(),
+                             _stream(stream)), "dspark_verify")
 
 
 def verify_gated(target, base, anchor, W1, gate, W2, tokens, q_tok, q_stats, sched_len, temperature, seed,
@@ -187,10 +203,11 @@ def verify_gated(target, base, anchor, W1, gate, W2, tokens, q_tok, q_stats, sch
     R, gamma, V = base.shape
     rank = W1.shape[1]
     _check(lib.dspark_verify_gated(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base),
-                                   _ptr(anchor), _ptr(W1), _ptr(gate), _ptr(W2), _ptr(tokens), _ptr(q_tok),
-                                   _ptr(q_stats), _ptr(sched_len), float(temperature), int(seed),
-                                   _ptr(out_tokens), _ptr(accepted_len), _ptr(p_tok), _ptr(ws), ws.numel(),
-                                   _stream(stream)), "dspark_verify_gated")
+                                   _ptr(anchor, _I32), _ptr(W1), _ptr(gate), _ptr(W2), _ptr(tokens, _I32),
+                                   _ptr(q_tok, _F32), _ptr(q_stats, _F32), _ptr(sched_len, _I32),
+                                   float(temperature), int(seed), _ptr(out_tokens, _I32), _ptr(accepted_len, _I32),
+                                   _ptr(p_tok, _F32), _ptr(ws, _U8), ws.numel(), _stream(stream)),
+           "dspark_verify_gated")
 
 
 def acceptance_labels(target, base, anchor, W1, W2, tokens, q_stats, temperature, labels, ws, stream=None):
@@ -198,9 +215,9 @@ def acceptance_labels(target, base, anchor, W1, W2, tokens, q_stats, temperature
     R, gamma, V = base.shape
     rank = W1.shape[1]
     _check(lib.dspark_acceptance_labels(R, gamma, V, rank, _dtype_code(base), _ptr(target), _ptr(base),
-                                        _ptr(anchor), _ptr(W1), _ptr(W2), _ptr(tokens), _ptr(q_stats),
-                                        float(temperature), _ptr(labels), _ptr(ws), ws.numel(), _stream(stream)),
-           "dspark_acceptance_labels")
+                                        _ptr(anchor, _I32), _ptr(W1), _ptr(W2), _ptr(tokens, _I32),
+                                        _ptr(q_stats, _F32), float(temperature), _ptr(labels, _F32), _ptr(ws, _U8),
+                                        ws.numel(), _stream(stream)), "dspark_acceptance_labels")
 
 
 def sts_fit(conf, accepted, grid, n_bins, temperature, ece=None, stream=None):
@@ -212,15 +229,16 @@ def sts_fit(conf, accepted, grid, n_bins, temperature, ece=None, stream=None):
     raw = torch.empty(n + 256, dtype=torch.uint8, device=conf.device)
     off = (-raw.data_ptr()) % 256
     scratch = raw[off:off + n]
-    _check(lib.dspark_sts_fit(N, gamma, _ptr(conf), _ptr(accepted), grid.numel(), _ptr(grid), n_bins,
-                              _ptr(temperature), _ptr(ece), _ptr(scratch), n, _stream(stream)), "dspark_sts_fit")
-    return int(lib.dspark_sts_status(_ptr(scratch), _stream(stream)))
+    _check(lib.dspark_sts_fit(N, gamma, _ptr(conf, _F32), _ptr(accepted, _I32), grid.numel(), _ptr(grid, _F32),
+                              n_bins, _ptr(temperature, _F32), _ptr(ece, _F32), _ptr(scratch, _U8), n,
+                              _stream(stream)), "dspark_sts_fit")
+    return int(lib.dspark_sts_status(_ptr(scratch, _U8), _stream(stream)))
 
 
 def sts_apply(conf, temperature, conf_out, stream=None):
     R, gamma = conf.shape
-    _check(lib.dspark_sts_apply(R, gamma, _ptr(conf), _ptr(temperature), _ptr(conf_out), _stream(stream)),
-           "dspark_sts_apply")
+    _check(lib.dspark_sts_apply(R, gamma, _ptr(conf, _F32), _ptr(temperature, _F32), _ptr(conf_out, _F32),
+                                _stream(stream)), "dspark_sts_apply")
 
 
 def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,
@@ -228,12 +246,13 @@ def round_(base, target, anchor, W1, W2, conf, conf_lagged, sps, mode, temperatu
     """One whole round; `out` is a RoundOutputs holding the output tensors."""
     R, gamma, V = base.shape
     rank = W1.shape[1]
-    _check(lib.dspark_round(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target), _ptr(anchor),
-                            _ptr(W1), _ptr(W2), _ptr(conf), _ptr(conf_lagged), _ptr(sps), sps.numel(),
-                            int(mode), float(temperature), int(seed), _ptr(out.tokens), _ptr(out.q_tok),
-                            _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K), _ptr(out.tau_theta),
-                            _ptr(out.out_tokens), _ptr(out.accepted_len), _ptr(out.p_tok), _ptr(ws),
-                            ws.numel(), _stream(stream)), "dspark_round")
+    _check(lib.dspark_round(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target), _ptr(anchor, _I32),
+                            _ptr(W1), _ptr(W2), _ptr(conf, _F32), _ptr(conf_lagged, _F32), _ptr(sps, _F32),
+                            sps.numel(), int(mode), float(temperature), int(seed), _ptr(out.tokens, _I32),
+                            _ptr(out.q_tok, _F32), _ptr(out.q_stats, _F32), _ptr(out.sched_len, _I32),
+                            _ptr(out.K, _I32), _ptr(out.tau_theta, _F64), _ptr(out.out_tokens, _I32),
+                            _ptr(out.accepted_len, _I32), _ptr(out.p_tok, _F32), _ptr(ws, _U8), ws.numel(),
+                            _stream(stream)), "dspark_round")
 
 
 def round_gated(base, target, anchor, W1, gate, W2, conf, conf_lagged, sps, mode, temperature, seed, out, ws,
@@ -241,30 +260,33 @@ def round_gated(base, target, anchor, W1, gate, W2, conf, conf_lagged, sps, mode
     """One whole round with the recurrent (gated) head."""
     R, gamma, V = base.shape
     rank = W1.shape[1]
-    _check(lib.dspark_round_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target), _ptr(anchor),
-                                  _ptr(W1), _ptr(gate), _ptr(W2), _ptr(conf), _ptr(conf_lagged), _ptr(sps),
-                                  sps.numel(), int(mode), float(temperature), int(seed), _ptr(out.tokens),
-                                  _ptr(out.q_tok), _ptr(out.q_stats), _ptr(out.sched_len), _ptr(out.K),
-                                  _ptr(out.tau_theta), _ptr(out.out_tokens), _ptr(out.accepted_len),
-                                  _ptr(out.p_tok), _ptr(ws), ws.numel(), _stream(stream)), "dspark_round_gated")
+    _check(lib.dspark_round_gated(R, gamma, V, rank, _dtype_code(base), _ptr(base), _ptr(target),
+                                  _ptr(anchor, _I32), _ptr(W1), _ptr(gate), _ptr(W2), _ptr(conf, _F32),
+                                  _ptr(conf_lagged, _F32), _ptr(sps, _F32), sps.numel(), int(mode),
+                                  float(temperature), int(seed), _ptr(out.tokens, _I32), _ptr(out.q_tok, _F32),
+                                  _ptr(out.q_stats, _F32), _ptr(out.sched_len, _I32), _ptr(out.K, _I32),
+                                  _ptr(out.tau_theta, _F64), _ptr(out.out_tokens, _I32),
+                                  _ptr(out.accepted_len, _I32), _ptr(out.p_tok, _F32), _ptr(ws, _U8), ws.numel(),
+                                  _stream(stream)), "dspark_round_gated")
 
 
 def copy_scheduled_rows(host_target, device_target, host_sched_len, stream=None):
     """Host-to-device copy of target rows 0..L_r of every request (host_target pinned)."""
     R, g1, V = host_target.shape
-    _check(lib.dspark_copy_scheduled_rows(R, g1 - 1, V, _dtype_code(host_target), _ptr(host_target),
-                                          _ptr(device_target), _ptr(host_sched_len), _stream(stream)),
+    _check(lib.dspark_copy_scheduled_rows(R, g1 - 1, V, _dtype_code(host_target),
+                                          _ptr(host_target, host=True), _ptr(device_target),
+                                          _ptr(host_sched_len, _I32, host=True), _stream(stream)),
            "dspark_copy_scheduled_rows")
 
 
 def wait_selftest(which, ws, stream=None):
     """A bounded device wait (0: grid barrier, 1: mbarrier) on a condition nothing meets; it
     gives up and records ERR_TIMEOUT in the workspace's status word."""
-    _check(lib.dspark_wait_selftest(int(which), _ptr(ws), ws.numel(), _stream(stream)), "dspark_wait_selftest")
+    _check(lib.dspark_wait_selftest(int(which), _ptr(ws, _U8), ws.numel(), _stream(stream)), "dspark_wait_selftest")
 
 
 def device_status(ws, stream=None):
-    return int(lib.dspark_device_status(_ptr(ws), _stream(stream)))
+    return int(lib.dspark_device_status(_ptr(ws, _U8), _stream(stream)))
 
 
 class RoundOutputs:

@@ -70,3 +70,20 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(os.path, "exists", lambda p: False if p.endswith("libdspark.so") else os.path.isfile(p))
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_binding_refuses_tensors_the_abi_cannot_describe():
+    """The C ABI takes dense arrays without strides: the binding refuses views
+    that are not contiguous, tensors on the wrong side of the host/device split
+    and, where an entry point fixes it, the wrong element type."""
+    torch = pytest.importorskip("torch")
+    from speculative_decoding_draft_seq_gb300 import dspark
+    assert dspark._ptr(None) is None
+    x = torch.zeros((4, 6), dtype=torch.int32)
+    assert dspark._ptr(x, torch.int32, host=True).value == x.data_ptr()
+    with pytest.raises(ValueError, match="contiguous"):
+        dspark._ptr(x.t(), host=True)
+    with pytest.raises(ValueError, match="CUDA"):
+        dspark._ptr(x)  # device arguments must be CUDA tensors
+    with pytest.raises(TypeError):
+        dspark._ptr(x.float(), torch.int32, host=True)
