@@ -44,6 +44,11 @@ constexpr uint32_t kPABytes = 4 * kPAChunk;
 constexpr uint32_t kPBBox = kPKC * 128;
 constexpr uint32_t kPBStage = 4 * kPBBox;
 constexpr uint32_t kPBaseBox = 128 * 128;
+// The 1 KB block after the rings holds the mbarriers and flags (204 bytes),
+// then, from byte 256, the draft uniforms of the CTA's first request.
+constexpr int kOddOffset = 256, kOddCap = 96;
+static_assert((2 * kPBStages + 4 * kPBaseStages + 10) * 8 + 12 <= kOddOffset && kOddOffset + 8 * kOddCap <= 1024,
+              "mbarriers, flags and the uniforms table fit the 1 KB block after the rings");
 constexpr uint32_t kPSmem = 1024 + kPABytes + kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox + 1024;
 constexpr uint32_t kGridSpinLimit = 1u << 20;  // about 1 s of polls
 
@@ -269,7 +274,7 @@ __device__ __forceinline__ void gated_advance(const PersistParams& p, int r, int
 // on w1Full, use number w1_use) while the chunk's logits are recomputed.
 template <bool kGated>
 __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* ls, int et, uint64_t* w1Full,
-                           uint32_t& w1_use) {
+                           uint32_t& w1_use, const uint64_t* odd_tab) {
   const int ew = et >> 5, lane = et & 31;
   float* sW1f = reinterpret_cast<float*>(ls + kLsW1);
   float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
@@ -355,7 +360,8 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       sW1f[i] = __uint_as_float((uint32_t)h << 16);
     }
   }
-  const uint64_t odd = philox_odd53(p.seed, (uint64_t)r, (uint64_t)k, kDraft);
+  // the draw's uniform: from the table filled at launch (this CTA's first request), else computed here
+  const uint64_t odd = odd_tab ? odd_tab[k - 1] : philox_odd53(p.seed, (uint64_t)r, (uint64_t)k, kDraft);
 
   float m = -INFINITY;
   if (cached) {
@@ -758,7 +764,7 @@ __device__ __forceinline__ void label_half_tma(const PersistParams& p, const Res
 // residual chunk sums: inverse CDF over the chunks, recompute of the crossing
 // chunk, float64 prefix within it. Falls back to P when the residual has no
 // mass.
-__device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* ls, int et) {
+__device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* ls, int et, const uint64_t* odd_tab) {
   const int ew = et >> 5, lane = et & 31;
   float* sW1f = reinterpret_cast<float*>(ls + kLsW1);
   float(*red)[64] = reinterpret_cast<float(*)[64]>(ls + kLsRed);
@@ -804,7 +810,8 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   if (use_p) excl = eg_exscan_u64(lp, shu, W, ew, lane, incl);
   const int kind = use_p ? kPendBonus : rr.kind;
   const uint64_t purpose = rr.kind == kPendResid ? kResid : kBonus;
-  const unsigned long long target = scale_u53(philox_odd53(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose), W);
+  const unsigned long long target =
+      scale_u53(odd_tab ? *odd_tab : philox_odd53(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose), W);
   if (et == 0) *sFlag = 1;
   eg_sync();
   int last_pos = -1;
@@ -962,7 +969,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kPBStages; ++i) { mbar_init(&bFull[i], 1); mbar_init(&bEmpty[i], 1); }
-    for (int i = 0; i < 2 * kPBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], 4); }
+    // base slots are released by the four warps of one epilogue half; the label pass's shared
+    // slots by all eight (every warp reads every chunk there)
+    const uint32_t empty_count = (kLabel && p.label_tma) ? kPEpiWarps : 4;
+    for (int i = 0; i < 2 * kPBaseStages; ++i) { mbar_init(&baseFull[i], 1); mbar_init(&baseEmpty[i], empty_count); }
     for (int i = 0; i < 2; ++i) { mbar_init(&accFull[i], 1); mbar_init(&accEmpty[i], kPEpiWarps); }
     for (int i = 0; i < 4; ++i) mbar_init(&aFull[i], 1);
     mbar_init(drain, 1);
@@ -1095,6 +1105,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // epilogue warps 3..10: A gather, softmax partials, grid barriers, locate
     const int et = tid - 96, ew = et >> 5;
     const bool ltma = kLabel && p.label_tma;  // label pass fed by TMA boxes (warp 2)
+    // Philox draws of the CTA's first request for every step, computed once here instead of on the
+    // draw's dependent path (many barriers pass before the first read)
+    uint64_t* sOdd = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(bars) + kOddOffset);
+    const bool odd_pre = !kResid && !p.greedy && p.gamma <= kOddCap && (int)blockIdx.x < p.R;
+    if (odd_pre && et < p.gamma) sOdd[et] = philox_odd53(p.seed, (uint64_t)blockIdx.x, (uint64_t)(et + 1), kDraft);
+    // residual pass: the one draw of the CTA's first request (its kind and position are inputs)
+    const bool odd_res = kResid && !kLabel && !p.greedy && (int)blockIdx.x < p.R;
+    if (odd_res && et == 0) {
+      const ResidRow r0 = load_resid_row(p, blockIdx.x);
+      if (r0.kind == kPendResid || r0.kind == kPendBonus)
+        sOdd[0] = philox_odd53(p.seed, (uint64_t)blockIdx.x, (uint64_t)(r0.A + 1),
+                               r0.kind == kPendResid ? Purpose::kResid : Purpose::kBonus);
+    }
     const int q = warp & 3, h = (warp - 3) >> 2;
     const int row = 32 * q + lane;
     const float kT = p.kT;
@@ -1203,7 +1226,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int c0 = c_begin + 4 * t, nbox = min(4, c_end - c0);
           if (!__all_sync(0xffffffffu, mbar_wait(&accFull[buf], use & 1, sAbort, p.status))) { stop = true; break; }
           tc_fence_after();
-          for (int j = h; j < nbox; j += 2) {
+          // label pass with TMA rows: every warp takes every chunk of the tile (its half h of the 64
+          // columns), so each warp waits on the shared slots in chunk order and is never more than
+          // one phase ahead of a slot's barrier; otherwise half h takes chunks h, h + 2
+          for (int j = ltma ? 0 : h; j < nbox; j += ltma ? 1 : 2) {
             if (kResid) {
               const int r = mt * kPM + row;
               float sw[4] = {0.f, 0.f, 0.f, 0.f}, sp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1214,11 +1240,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                   break;
                 }
                 const unsigned char* sl = sBase + (size_t)slot * kLSlotBytes;
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh)
-                  label_half_tma(p, rr, (c0 + j) * 64 + 32 * hh,
-                                 tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * hh), sl,
-                                 row, hh, sw);
+                label_half_tma(p, rr, (c0 + j) * 64 + 32 * h,
+                               tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64 + 32 * h), sl, row,
+                               h, sw);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&baseEmpty[slot]);
               } else {
@@ -1253,15 +1277,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int am = 0x7fffffff;
             uint32_t accr[64];
             __syncwarp();
-            // the accumulator load lands while the base logits are read from shared memory;
-            // both buffers are released as soon as their values are in registers
+            // the accumulator load lands while the base logits are read from shared memory; the
+            // accumulator is released as soon as its values are in registers, the base slot only
+            // once its values have been used (released right after the loads, with the arithmetic
+            // still to come, some drafts read a slot the next box had already overwritten)
             tmem_ld64_nowait(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), accr);
             uint4 bx[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) bx[u] = *reinterpret_cast<const uint4*>(brow + ((u ^ (row & 7)) << 4));
-            tmem_ld_wait();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&baseEmpty[s]);
+            tmem_ld_wait64(accr);
             if (j + 2 >= nbox) {  // this half's last chunk of the tile: the accumulator is free
               tc_fence_before();
               __syncwarp();
@@ -1303,6 +1327,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
               for (int i = 0; i < 64; ++i) sq[i & 7] += pweight(l[i], kT, mk);
               ssum = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&baseEmpty[s]);
             const int r = mt * kPM + row;
             if (r < p.R)
               __stcg(p.part + (size_t)r * p.nc + (c0 + j),
@@ -1337,9 +1363,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       for (int r = blockIdx.x; r < p.R; r += p.n_cta) {
         if (kResid)
-          locate_resid_row(p, r, sA, et);
+          locate_resid_row(p, r, sA, et, (odd_res && r == (int)blockIdx.x) ? sOdd : nullptr);
         else
-          locate_row<kGated>(p, r, k, sA, et, w1Full, w1_use);
+          locate_row<kGated>(p, r, k, sA, et, w1Full, w1_use, (odd_pre && r == (int)blockIdx.x) ? sOdd : nullptr);
         eg_sync();
       }
       if (!kResid) {

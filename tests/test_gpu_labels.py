@@ -78,3 +78,29 @@ def test_labels_full_size_sampled():
     ref = _oracle_labels(cfg, tokens, [0, 64, 127])
     for r, v in ref.items():
         np.testing.assert_allclose(lab[r], v, rtol=0, atol=LABEL_ATOL)
+
+
+@pytest.mark.parametrize("cfg", [W.CONFIGS["ds"], SHAPES[2]], ids=["ds", "lab_rows"])
+def test_labels_repeat_bit_for_bit(cfg):
+    """The label pass run many times on the same inputs (L2 flushed between
+    runs, as a timing loop does) gives the same bits every time: the sums are
+    exact integers, so any difference would be a race in the row staging."""
+    from speculative_decoding_draft_seq_gb300 import dspark
+    inp = W.device_inputs(cfg, "cuda")
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, inp["W1"].shape[1], dspark.BF16, inp["sps"].numel())
+    out = dspark.RoundOutputs(R, gamma)
+    dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"], out.tokens,
+                            out.q_tok, out.q_stats, ws)
+    labels = torch.empty((R, gamma), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    first = None
+    for _ in range(60):
+        flush.zero_()
+        dspark.acceptance_labels(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], out.tokens,
+                                 out.q_stats, inp["T"], labels, ws)
+        if first is None:
+            first = labels.clone()
+        else:
+            assert torch.equal(labels, first)
+    assert dspark.device_status(ws) == dspark.OK

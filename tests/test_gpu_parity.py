@@ -167,6 +167,32 @@ def test_deterministic_bits():
         assert np.array_equal(a[k], b[k]), k
 
 
+
+def test_full_size_drafts_repeat_bit_for_bit():
+    """The DeepSeek-scale draft run many times on the same inputs (L2 flushed
+    between runs, as a timing loop does) gives the same bits every time. The
+    chunk partials are combined exactly, so any difference is a race in the
+    staging of the sweep (an early-released base slot showed up here as one
+    draft in five with a slightly different normaliser)."""
+    cfg = W.CONFIGS["ds"]
+    inp = device_inputs(cfg)
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dspark.BF16, cfg.n_table)
+    out = dspark.RoundOutputs(R, gamma)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ref = None
+    for _ in range(40):
+        flush.zero_()
+        dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"], out.tokens,
+                                out.q_tok, out.q_stats, ws)
+        cur = (out.tokens.clone(), out.q_tok.clone(), out.q_stats.clone())
+        if ref is None:
+            ref = cur
+        else:
+            assert all(torch.equal(a, b) for a, b in zip(cur, ref))
+    assert dspark.device_status(ws) == dspark.OK
+
+
 TC_SWEEP = [
     # (R, gamma, V, rank): the tensor-core drafting sweep and residual pass at other shapes
     (200, 3, 2056, 128),   # 200 requests: two M tiles, CTAs drawing two requests per step
