@@ -648,8 +648,10 @@ static_assert(2 * kPBStage + kPEpiWarps * kRsWarpBytes <= kPBStages * kPBStage +
 // base logits viewed as [R * gamma][V], and its target rows one box of the
 // target logits [R][gamma + 1][V] taking gamma positions of 128 / gamma
 // requests. Three slots of (target box, base box) in the staging region,
-// filled by warp 2 in chunk order and released by the four warps of the
-// epilogue half that reads them.
+// filled by warp 2 in chunk order. Every epilogue warp reads every chunk (its
+// 32-column half) in the same order and the eight release the slot, so no
+// warp ever waits on a slot's barrier more than one phase ahead (a parity
+// wait cannot tell a phase two ahead from a completed one).
 constexpr int kLSlots = 3;
 constexpr uint32_t kLSlotBytes = 2 * kPBaseBox;
 static_assert(kLSlots * kLSlotBytes <= kPEpiWarps * kRsWarpBytes, "the label slots fit the staging region");
