@@ -193,6 +193,36 @@ def test_full_size_drafts_repeat_bit_for_bit():
     assert dspark.device_status(ws) == dspark.OK
 
 
+
+@pytest.mark.parametrize("gated", [False, True], ids=["markov", "gated"])
+def test_full_size_rounds_repeat_bit_for_bit(gated):
+    """Whole DeepSeek-scale rounds (draft, schedule, verify with its residual
+    pass) repeated with L2 flushed between them give the same bits every time,
+    for the Markov and the gated head."""
+    cfg = W.with_(W.CONFIGS["ds"], gated=True) if gated else W.CONFIGS["ds"]
+    inp = device_inputs(cfg)
+    gate = W.gate_device(cfg, "cuda") if gated else None
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dspark.BF16, cfg.n_table)
+    out = dspark.RoundOutputs(R, gamma)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ref = None
+    for _ in range(20):
+        flush.zero_()
+        if gated:
+            dspark.round_gated(inp["base"], inp["target"], inp["anchor"], inp["W1"], gate, inp["W2"], inp["conf"],
+                               inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+        else:
+            dspark.round_(inp["base"], inp["target"], inp["anchor"], inp["W1"], inp["W2"], inp["conf"],
+                          inp["conf_lag"], inp["sps"], inp["mode"], inp["T"], inp["seed"], out, ws)
+        cur = [t.clone() for t in vars(out).values()]
+        if ref is None:
+            ref = cur
+        else:
+            assert all(torch.equal(a, b) for a, b in zip(cur, ref))
+    assert dspark.device_status(ws) == dspark.OK
+
+
 TC_SWEEP = [
     # (R, gamma, V, rank): the tensor-core drafting sweep and residual pass at other shapes
     (200, 3, 2056, 128),   # 200 requests: two M tiles, CTAs drawing two requests per step
