@@ -5,6 +5,7 @@ into one shared object next to this file, against the shared CUDA runtime so
 that the process's runtime (e.g. the one PyTorch loaded) is reused.
 """
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -43,10 +44,22 @@ def up_to_date():
 
 
 def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link; returns the path of libdspark.so."""
+    """Compile and link; returns the path of libdspark.so. Several processes (one per rank) may call
+    it at once: a file lock lets one build while the others wait and then find the library fresh."""
     if not force and up_to_date():
         return OUT
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return OUT
+            return _build_locked(verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose, extra_flags):
     cc = nvcc()
 
     def compile_one(src):
