@@ -45,10 +45,13 @@ constexpr uint32_t kPBBox = kPKC * 128;
 constexpr uint32_t kPBStage = 4 * kPBBox;
 constexpr uint32_t kPBaseBox = 128 * 128;
 // The 1 KB block after the rings holds the mbarriers and flags (204 bytes),
-// then, from byte 256, the draft uniforms of the CTA's first request.
-constexpr int kOddOffset = 256, kOddCap = 96;
-static_assert((2 * kPBStages + 4 * kPBaseStages + 10) * 8 + 12 <= kOddOffset && kOddOffset + 8 * kOddCap <= 1024,
-              "mbarriers, flags and the uniforms table fit the 1 KB block after the rings");
+// from byte 208 one scratch word per epilogue warp (the stores that hold a
+// base slot's release until its values are in registers), and from byte 256
+// the draft uniforms of the CTA's first request.
+constexpr int kDepOffset = 208, kOddOffset = 256, kOddCap = 96;
+static_assert((2 * kPBStages + 4 * kPBaseStages + 10) * 8 + 12 <= kDepOffset &&
+                  kDepOffset + 4 * kPEpiWarps <= kOddOffset && kOddOffset + 8 * kOddCap <= 1024,
+              "mbarriers, flags, scratch words and the uniforms table fit the 1 KB block after the rings");
 constexpr uint32_t kPSmem = 1024 + kPABytes + kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox + 1024;
 constexpr uint32_t kGridSpinLimit = 1u << 20;  // about 1 s of polls
 
@@ -1279,15 +1282,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int am = 0x7fffffff;
             uint32_t accr[64];
             __syncwarp();
-            // the accumulator load lands while the base logits are read from shared memory; the
-            // accumulator is released as soon as its values are in registers, the base slot only
-            // once its values have been used (released right after the loads, with the arithmetic
-            // still to come, some drafts read a slot the next box had already overwritten)
+            // the accumulator load lands while the base logits are read from shared memory; both
+            // buffers are given back as soon as their values are in registers. For the base slot
+            // that is made explicit: each lane first stores a value that needs all eight of its
+            // loads, and the release (which orders stores) follows the warp's stores. Releasing
+            // right after the loads were issued let some drafts read a slot the next box had
+            // already overwritten.
             tmem_ld64_nowait(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256 + j * 64), accr);
             uint4 bx[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) bx[u] = *reinterpret_cast<const uint4*>(brow + ((u ^ (row & 7)) << 4));
             tmem_ld_wait64(accr);
+            {
+              uint32_t dep = 0;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) dep ^= bx[u].x ^ bx[u].w;
+              *reinterpret_cast<volatile uint32_t*>(reinterpret_cast<unsigned char*>(bars) + kDepOffset + 4 * ew) = dep;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&baseEmpty[s]);
+            }
             if (j + 2 >= nbox) {  // this half's last chunk of the tile: the accumulator is free
               tc_fence_before();
               __syncwarp();
@@ -1329,8 +1342,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
               for (int i = 0; i < 64; ++i) sq[i & 7] += pweight(l[i], kT, mk);
               ssum = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&baseEmpty[s]);
             const int r = mt * kPM + row;
             if (r < p.R)
               __stcg(p.part + (size_t)r * p.nc + (c0 + j),
