@@ -606,7 +606,7 @@ def main():
     traffic = measured_traffic(dominant)
     line = {
         "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "round_us": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": workload, "l2": "flushed between steps (256 MiB write, outside the events)",
                    "parallelism": (f"request-sharded x{world}: local draft and verify, all-gathered "
