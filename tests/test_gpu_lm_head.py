@@ -66,11 +66,13 @@ def _run(cfg, d, dev="cuda"):
 
 @pytest.mark.parametrize("M,d,V", [
     (1, 64, 64),        # one row, one K step, one column box
-    (256, 64, 64),      # two row tiles (one CTA pair), one column box
+    (256, 64, 64),      # one full 256-row tile (both 128-row halves), one column box
+    (129, 128, 128),    # the second half of the tile holds a single row
     (200, 512, 1000),   # a partial row tile and a partial last column box
     (5, 64, 72),        # fewer rows than a tile, two column boxes
     (128, 136, 256),    # a K tail of 8
-    (300, 7168, 512),   # the DeepSeek hidden size
+    (520, 192, 320),    # three row tiles, the last with an empty second half
+    (300, 7168, 512),   # the DeepSeek hidden size; the second row tile is partial
 ])
 def test_lm_head_matches_oracle(M, d, V):
     cfg = W.Workload(f"lm_{M}_{d}_{V}", R=M, gamma=1, V=V, rank=64, dtype="bf16", T=1.0, mode=W.CAUSAL,
@@ -149,7 +151,7 @@ def test_draft_from_hidden_states():
 def test_lm_head_qwen_shape_sampled():
     """A second model shape: Qwen3-4B's hidden size (2560) and vocabulary
     (151,936, not a multiple of 256: a partial last column tile), a 7-token
-    block over 32 requests (two row tiles in one CTA pair)."""
+    block over 32 requests (224 rows: one row tile, its second half partial)."""
     cfg = W.Workload("lm_qwen", R=32, gamma=7, V=151936, rank=64, dtype="bf16", T=1.0, mode=W.CAUSAL, seed=6200)
     d = 2560
     H, LM, out = _run(cfg, d)
