@@ -104,9 +104,11 @@ dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes,
  *   q_tok        [R, gamma] float out  Q_k(x_k), the draft probability of x_k
  *   q_stats      [R, gamma, 2] float out  (M, Z): Q_k(v) = 2^((l_v - M) log2(e)/T) / Z
  *                                         (greedy: (max l, 1))
- * Requirements: R >= 1, gamma >= 1, V >= 1, rank >= 1. The bf16 tensor-core
- * path is used when dtype = BF16, rank % 16 == 0, rank <= 256, V % 8 == 0;
- * other shapes run on CUDA cores with the same results up to rounding.
+ * Requirements: R >= 1, gamma >= 1, V >= 1, rank >= 1. The tensor-core path
+ * (one cooperative launch for all gamma steps) is used when dtype = BF16,
+ * rank % 64 == 0, rank <= 256, V % 8 == 0, V >= 64, base_logits, W1 and W2
+ * are 16-byte aligned and the device supports cooperative launch; other
+ * shapes run on CUDA cores with the same results up to rounding.
  */
 dspark_status dspark_draft_sequential(int32_t R, int32_t gamma, int32_t V, int32_t rank,
                                       int32_t dtype, const void* base_logits,

@@ -10,17 +10,13 @@
 namespace dspark {
 bool draft_tc_eligible(const DraftArgs& a);
 cudaError_t launch_draft_cuda_core(const DraftArgs& a, cudaStream_t s, int& launches);
-cudaError_t launch_draft_tc(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken);
 cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken);
 
 // bf16 shapes the tensor cores take run as one persistent cooperative launch
-// (all steps); the per-step tensor-core kernels serve them when a cooperative
-// launch is not possible; every other shape runs on CUDA cores.
+// (all steps); every other shape runs on CUDA cores.
 cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches) {
   bool taken = false;
   cudaError_t e = launch_draft_persistent(a, s, launches, taken);
-  if (taken || e != cudaSuccess) return e;
-  e = launch_draft_tc(a, s, launches, taken);
   if (taken || e != cudaSuccess) return e;
   return launch_draft_cuda_core(a, s, launches);
 }

@@ -155,10 +155,25 @@ __global__ void __launch_bounds__(256) draft_locate_kernel(
       if (p.x > bv || (p.x == bv && idx < bi)) { bv = p.x; bi = idx; }
     }
     block_argmax(bv, bi, shf, shi);
+    // The recorded maximum is the drafted token's logit with its bias summed in
+    // float64 and rounded once, fl32(base + fl32(W1[prev] . W2[:, x])): the value
+    // the greedy argmax is defined on (the float32 sums the argmax was taken over
+    // can differ from it in the last bits). Every product of two float32 inputs
+    // is exact in float64.
+    const int x = min(max(bi, 0), V - 1);
+    const int prev = draft_prev(k, r, gamma, V, anchor, tokens, status);
+    double acc = 0.0;
+    for (int i = tid; i < rank; i += blockDim.x)
+      acc = fma((double)ld_elem(W1, (size_t)prev * rank + i), (double)ld_elem(W2, (size_t)i * V + x), acc);
+    acc = warp_sum_d(acc);
+    if ((tid & 31) == 0) shd[tid >> 5] = acc;
+    __syncthreads();
     if (tid == 0) {
+      double bias = 0.0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) bias += shd[w];
       tokens[out] = bi;
       q_tok[out] = 1.f;
-      q_stats[2 * out] = bv;
+      q_stats[2 * out] = __fadd_rn(ld_elem(base, ((size_t)r * gamma + (k - 1)) * V + x), __double2float_rn(bias));
       q_stats[2 * out + 1] = 1.f;
     }
     return;

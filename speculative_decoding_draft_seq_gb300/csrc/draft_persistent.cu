@@ -336,10 +336,35 @@ __device__ void locate_row(const PersistParams& p, int r, int k, unsigned char* 
       }
       fence_proxy_async_global();
     }
+    if (ew == 1) {
+      // The recorded maximum is the drafted token's logit with its bias summed
+      // in float64 and rounded once, fl32(base + fl32(a . W2[:, tok])), a = this
+      // step's A row (W1[prev], or the gated head's bf16 state): the value the
+      // greedy argmax is defined on. The tensor cores' float32 sums, which the
+      // argmax was taken over, can differ from it in the last bits. Products of
+      // two bf16 values are exact in float64.
+      double acc = 0.0;
+      const int a = min(max(__ldg(p.anchor + r), 0), p.V - 1);
+      const unsigned short* arow =
+          reinterpret_cast<const unsigned short*>(p.astage + ((size_t)((k - 1) & 1) * p.R + r) * p.rank);
+      for (int i = lane; i < p.rank; i += 32) {
+        float av;
+        if (k > 1) {
+          av = __uint_as_float((uint32_t)__ldcg(arow + i) << 16);
+        } else {
+          av = __bfloat162float(p.W1[(size_t)a * p.rank + i]);
+          if (kGated) av = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__bfloat162float(p.gate[(size_t)a * p.rank + i]), av)));
+        }
+        acc = fma((double)av, (double)__bfloat162float(p.W2[(size_t)i * p.V + tok]), acc);
+      }
+      acc = warp_sum_d(acc);
+      if (lane == 0)
+        p.q_stats[2 * out] = __fadd_rn(__bfloat162float(p.base[((size_t)r * p.gamma + (k - 1)) * p.V + tok]),
+                                       __double2float_rn(acc));
+    }
     if (et == 0) {
       __stcg(p.tokens + out, tok);
       p.q_tok[out] = 1.f;
-      p.q_stats[2 * out] = bv;
       p.q_stats[2 * out + 1] = 1.f;
     }
     fence_proxy_async_smem();  // the scratch is overwritten next by a TMA load of the A operand
@@ -1410,7 +1435,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 namespace dspark {
 
-bool draft_tc_eligible(const DraftArgs& a);
+// Shapes the tensor-core sweep takes: bf16, rank a multiple of 64 up to 256
+// (whole 64-column K boxes of A, at most 8 rows per thread in the draw), V a
+// multiple of 8 (16-byte TMA row strides) and at least 64 (one column box),
+// and 16-byte aligned tensors.
+bool draft_tc_eligible(const DraftArgs& a) {
+  return a.dtype == DSPARK_BF16 && a.rank % 64 == 0 && a.rank <= 256 && a.V % 8 == 0 && a.V >= 64 &&
+         (reinterpret_cast<uintptr_t>(a.base) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.W1) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.W2) & 15) == 0;
+}
 
 cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& launches, bool& taken) {
   taken = false;
