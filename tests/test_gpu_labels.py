@@ -68,14 +68,15 @@ def test_greedy_labels_are_exact(cfg):
         np.testing.assert_array_equal(lab[r], ref[r].astype(np.float32))
 
 
-def test_labels_full_size_sampled():
-    """DeepSeek-scale (R = 128, gamma = 16, V = 129280): every label in [0, 1],
-    and sampled requests (first, middle, last) against the oracle."""
+def test_labels_full_size_every_request():
+    """DeepSeek-scale (R = 128, gamma = 16, V = 129280): every label of every
+    request against the oracle."""
+    import oracle_pool
     cfg = W.CONFIGS["ds"]
     inp = W.device_inputs(cfg, "cuda")
     tokens, lab, _ = _device_labels(cfg, inp)
     assert np.all((lab >= 0) & (lab <= 1))
-    ref = _oracle_labels(cfg, tokens, [0, 64, 127])
+    ref = oracle_pool.oracle_labels(cfg, tokens, list(range(cfg.R)))
     for r, v in ref.items():
         np.testing.assert_allclose(lab[r], v, rtol=0, atol=LABEL_ATOL)
 

@@ -1,9 +1,10 @@
 """GPU parity: the CUDA library (called through its C ABI) against the oracle.
 
-Small cases compare every request; the full-size workloads run the whole round
-on the device in the configuration the benchmark times and compare sampled
-requests (the oracle drafts and verifies them one by one; the schedule is
-always compared in full).
+Every case compares every request, except the 1,024-request scheduler stress
+workload (128 requests spread over its eight M tiles); the full-size
+workloads run the whole round on the device in the configuration the
+benchmark times, and the oracle's per-request work is spread over host
+processes (tests/oracle_pool.py). The schedule is always compared in full.
 """
 import json
 import os
@@ -18,6 +19,7 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
+    import oracle_pool
     from gpu_harness import compare, device_inputs, gpu_round, oracle_round
     from speculative_decoding_draft_seq_gb300 import dspark
 
@@ -66,23 +68,36 @@ def test_small_vocab_greedy():
     _full(W.with_(W.CONFIGS["small"], T=0.0))
 
 
-@pytest.mark.parametrize("name,T,requests", [
-    ("ds", 1.0, [0, 77, 127]),
-    ("ds", 0.0, [5, 126]),
-    ("mixed", 1.0, [0, 127, 128, 255]),
-    ("mixed", 0.0, [1, 200]),
-    ("stress", 1.0, [0, 513, 1023]),
-])
-def test_full_size_sampled(name, T, requests):
-    cfg = W.with_(W.CONFIGS[name], T=T)
-    g = gpu_round(cfg)
-    o = oracle_round(cfg, requests)
-    rep = compare(cfg, g, o, requests)
+def _stress_requests():
+    """128 of the 1,024 stress requests: 16 in each of the eight 128-request M tiles, at offsets that
+    differ from tile to tile (first and last rows of a tile included)."""
+    return [mt * 128 + j for mt in range(8) for j in sorted({(mt + 8 * i) % 128 for i in range(15)} | {127})][:128]
+
+
+def record(workload, T, requests, rep):
     rep = {k: (float(v) if isinstance(v, (float, np.floating)) else v) for k, v in rep.items()}
     out_dir = os.environ.get("DSPARK_OUT_DIR", "runs")
     os.makedirs(out_dir, exist_ok=True)
     with open(os.path.join(out_dir, "parity_reports.jsonl"), "a") as f:
-        f.write(json.dumps({"workload": name, "T": T, "requests": requests, **rep}) + "\n")
+        f.write(json.dumps({"workload": workload, "T": T, "n_requests": len(requests), **rep}) + "\n")
+    print(f"{workload} T={T}: {rep}")
+    return rep
+
+
+@pytest.mark.parametrize("name,T", [("ds", 1.0), ("ds", 0.0), ("mixed", 1.0), ("mixed", 0.0), ("stress", 1.0)])
+def test_full_size_every_request(name, T):
+    """The full-size round in the benchmark's launch configuration, compared
+    with the oracle on every request (DeepSeek-scale and both halves of the
+    mixed-domain batch), or on 128 requests spread over all eight M tiles
+    (scheduler stress, 1,024 requests); the schedule is compared in full."""
+    cfg = W.with_(W.CONFIGS[name], T=T)
+    requests = _stress_requests() if name == "stress" else list(range(cfg.R))
+    g = gpu_round(cfg)
+    o = oracle_pool.oracle_round(cfg, requests)
+    rep = record(name, T, requests, compare(cfg, g, o, requests))
+    if T > 0:  # the corrected token after a rejection ([GN] "Definição do problema": G rejected, G* drawn)
+        assert rep["resid_compared"] >= (30 if name == "ds" else 60), rep
+    assert rep["bonus_compared"] > 0, rep
 
 
 def test_full_size_invariants_ds():
