@@ -51,3 +51,20 @@ def test_norm_table_is_symmetric_gaussian_quantiles():
     assert q.shape == (65536,)
     np.testing.assert_array_equal(q[:32768], -q[::-1][:32768])
     assert abs(float(np.std(q.astype(np.float64))) - 1.0) < 2e-3
+
+
+def test_host_built_inputs_equal_the_device_generator():
+    """device_inputs_from_host (numpy + one copy per tensor, used by smoke())
+    gives the same tensors as the torch generator, here both on the CPU."""
+    torch = pytest.importorskip("torch")
+    for cfg in (W.with_(W.CONFIGS["small"], R=3, V=640, rank=64, gated=True), W.CONFIGS["tiny"]):
+        a = W.device_inputs(cfg, "cpu")
+        b = W.device_inputs_from_host(cfg, "cpu")
+        assert a.keys() == b.keys()
+        for k, v in a.items():
+            if isinstance(v, torch.Tensor):
+                assert v.dtype == b[k].dtype and v.shape == b[k].shape, k
+                assert torch.equal(v.view(torch.int16) if v.dtype == torch.bfloat16 else v,
+                                   b[k].view(torch.int16) if v.dtype == torch.bfloat16 else b[k]), k
+            else:
+                assert v == b[k], k

@@ -460,3 +460,26 @@ def device_inputs(cfg, device="cuda"):
     return dict(base=base, target=target, W1=W1, W2=W2, anchor=t(h["anchor"]), conf=t(h["conf"]),
                 conf_lag=t(h["conf_lag"]), sps=t(h["sps"]), T=cfg.T, seed=cfg.philox_seed,
                 mode=cfg.mode, gate=gate_device(cfg, device) if cfg.gated else None)
+
+
+def device_inputs_from_host(cfg, device="cuda"):
+    """The same inputs as device_inputs, generated with numpy on the host and
+    copied to the device with one copy per tensor (no generator kernels run on
+    the device). Meant for small workloads: every request's rows are built on
+    the host."""
+    torch = _torch()
+    base, tgt = logits_rows_np(cfg, range(cfg.R))
+    W1, W2 = weights_np(cfg)
+    h = host_inputs(cfg)
+
+    def dev(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:  # bf16 bit patterns
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(a).to(device)
+
+    return dict(base=dev(base), target=dev(tgt), W1=dev(W1), W2=dev(W2), anchor=dev(h["anchor"]),
+                conf=dev(h["conf"]), conf_lag=dev(h["conf_lag"]), sps=dev(h["sps"]), T=cfg.T,
+                seed=cfg.philox_seed, mode=cfg.mode, gate=dev(gate_np(cfg)) if cfg.gated else None)
