@@ -110,35 +110,113 @@ def host_cpu_model():
 
 
 class ClockSampler:
+    """SM clock, power and clock-event reasons sampled during the timed region.
+
+    Reads NVML directly (ctypes on the driver's libnvidia-ml) from a background
+    thread about once a millisecond, so that even a timed region of a few
+    milliseconds gets several samples; falls back to `nvidia-smi -lms 25` when
+    NVML cannot be loaded. Only reads: no clock or other setting is touched.
+    Each sample is written to clocks_rank<r>.csv in $DSPARK_OUT_DIR (or runs/)."""
+    # clock-event reason bits of NVML
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
     def __init__(self):
         self.proc = None
         self.path = None
+        self.thread = None
+        self.rows = []
+        self.max_mhz = None
+
+    def _nvml_handle(self, index):
+        import ctypes
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                pass
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        try:  # the device this process runs on, by PCI address (NVML's index order may differ from CUDA's)
+            import torch
+            pr = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0:
+                return lib, h
+        except Exception:
+            pass
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+            return None, None
+        return lib, h
 
     def start(self, rank):
+        import threading
         out_dir = os.environ.get("DSPARK_OUT_DIR", os.path.join(ROOT, "runs"))
         os.makedirs(out_dir, exist_ok=True)
         self.path = os.path.join(out_dir, f"clocks_rank{rank}.csv")
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0] or "0"
+        index = int(dev) if dev.isdigit() else rank
+        lib, h = self._nvml_handle(index)
+        if lib is None:
+            return self._start_smi(index)
+        import ctypes
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.stop_flag = threading.Event()
+
+        def loop():
+            clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self.stop_flag.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    p_ok = lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0
+                    r_ok = get_reasons(h, ctypes.byref(rs)) == 0
+                    self.rows.append((time.time(), float(clk.value), pw.value / 1000.0 if p_ok else None,
+                                      int(rs.value) if r_ok else 0))
+                time.sleep(0.001)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+        t0 = time.time()  # the first sample exists before the timed region starts
+        while not self.rows and time.time() - t0 < 2.0:
+            time.sleep(0.001)
+
+    def _start_smi(self, index):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0] or "0"
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(rank if not dev.isdigit() else dev),
-                                          f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                          "-lms", "25"], stdout=open(self.path, "w"),
-                                         stderr=subprocess.DEVNULL)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
             return
-        # nvidia-smi needs a moment before its first line: wait for it (at most
-        # 5 s) so that the samples cover the timed region that follows
-        t0 = time.time()
+        t0 = time.time()  # nvidia-smi needs a moment before its first line
         while time.time() - t0 < 5.0:
             if os.path.getsize(self.path) > 0:
                 break
             time.sleep(0.02)
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join()
+            rows = self.rows
+            if not rows:
+                return None
+            with open(self.path, "w") as f:
+                f.write("time_s,sm_mhz,power_w,reasons_mask\n")
+                for t, c, pw, rs in rows:
+                    f.write(f"{t:.6f},{c:.0f},{'' if pw is None else f'{pw:.1f}'},{rs:#x}\n")
+            sm = sorted(r[1] for r in rows)
+            reasons = sorted({n for r in rows for bit, n in self.REASONS.items() if r[3] & bit})
+            return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                    "samples": len(rows), "source": "nvml"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -159,7 +237,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": sm[len(sm) // 2] if sm else None,
                 "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi"}
 
 
 # DRAM bytes per launch of the persistent drafting / residual kernel, from

@@ -52,8 +52,10 @@ def _static(cfg, dev, conf_override=None):
     return L.cpu().numpy(), K.cpu().numpy(), tt.cpu().numpy(), int(st.item())
 
 
-CASES = [W.CONFIGS["stress"],                       # R * gamma = 16384, the scratch maximum, LAGGED
+CASES = [W.CONFIGS["stress"],                       # R * gamma = 16384, the scratch maximum, LAGGED (radix form)
          W.CONFIGS["ds"],                           # CAUSAL
+         W.with_(W.CONFIGS["ds"], mode=W.LAGGED),   # LAGGED on the small form: its lagged Theta by position
+                                                    # shares bytes with the radix form's keys
          W.with_(W.CONFIGS["mixed"], mode=W.ALL),   # ALL
          W.CONFIGS["mixed"]]                        # CAUSAL again, after a smaller problem
 
