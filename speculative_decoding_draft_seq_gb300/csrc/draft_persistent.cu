@@ -804,13 +804,9 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   unsigned long long* sExcl = reinterpret_cast<unsigned long long*>(ls + kLsExcl);
   int* sFlag = reinterpret_cast<int*>(ls + kLsFlag);
 
-  const ResidRow rr = load_resid_row(p, r);
-  if (rr.kind == kPendNone) return;  // same for every thread of the group
-  if (rr.kind == kPendResid) {  // the A row the verifier staged: W1[prev], or bf16(s_j) for the gated head
-    const unsigned short* arow = reinterpret_cast<const unsigned short*>(p.astage + (size_t)r * p.rank);
-    for (int i = et; i < p.rank; i += kPEpiThreads) sW1f[i] = __uint_as_float((uint32_t)__ldcg(arow + i) << 16);
-  }
-
+  // the chunk sums, the request's pending record and the staged A row (W1[prev], or bf16(s_j) for the
+  // gated head; rank <= 256, one element per thread) are independent loads: all issued first, the A row
+  // kept in a register until the crossing chunk's bias needs it
   const int nc = p.nc;
   const float2* pr = p.rpart + (size_t)r * nc;
   unsigned long long* shu = shd;
@@ -822,6 +818,10 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
 #pragma unroll
   for (int i = 0; i < kCache; ++i)
     cache[i] = (cached && i < c1 - c0) ? __ldcg(pr + c0 + i) : make_float2(0.f, 0.f);
+  const uint32_t a_bits =
+      et < p.rank ? (uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(p.astage + (size_t)r * p.rank) + et) : 0u;
+  const ResidRow rr = load_resid_row(p, r);
+  if (rr.kind == kPendNone) return;  // same for every thread of the group
   auto getp = [&](int i) -> float2 { return cached ? cache[i] : __ldcg(pr + c0 + i); };
   unsigned long long lres = 0ull, lp = 0ull;
   if (cached) {
@@ -843,6 +843,7 @@ __device__ void locate_resid_row(const PersistParams& p, int r, unsigned char* l
   const unsigned long long target =
       scale_u53(odd_tab ? *odd_tab : philox_odd53(p.seed, (uint64_t)r, (uint64_t)(rr.A + 1), purpose), W);
   if (et == 0) *sFlag = 1;
+  if (rr.kind == kPendResid && et < p.rank) sW1f[et] = __uint_as_float(a_bits << 16);
   eg_sync();
   int last_pos = -1;
   if (cached) {

