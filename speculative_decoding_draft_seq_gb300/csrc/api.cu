@@ -213,8 +213,12 @@ static dspark_status round_entry(int32_t R, int32_t gamma, int32_t V, int32_t ra
     return DSPARK_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int n = 0;
+  // the schedule's inputs do not depend on the draft: the tensor-core drafting launch computes it as its
+  // last phase when the problem is small, else the scheduler runs as its own launch
+  ScheduleArgs sa{R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta, workspace};
+  bool sched_done = false;
   DraftArgs da{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, temperature, seed,
-               draft_tokens, q_tok, q_stats, workspace, gate};
+               draft_tokens, q_tok, q_stats, workspace, gate, &sa, &sched_done};
   cudaError_t e;
   if (gate) {
     bool taken = false;
@@ -223,10 +227,7 @@ static dspark_status round_entry(int32_t R, int32_t gamma, int32_t V, int32_t ra
   } else {
     e = launch_draft(da, s, n);
   }
-  if (e == cudaSuccess) {
-    ScheduleArgs sa{R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta, workspace};
-    e = launch_schedule(sa, s, n);
-  }
+  if (e == cudaSuccess && !sched_done) e = launch_schedule(sa, s, n);
   if (e == cudaSuccess) {
     VerifyArgs va{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens,
                   q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace, gate};

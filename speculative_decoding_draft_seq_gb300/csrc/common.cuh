@@ -183,6 +183,11 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
 }
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 __device__ __forceinline__ int warp_min_i(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));

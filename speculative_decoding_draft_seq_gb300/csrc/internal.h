@@ -9,6 +9,8 @@
 
 namespace dspark {
 
+struct ScheduleArgs;
+
 struct DraftArgs {
   int R, gamma, V, rank, dtype;
   const void* base;
@@ -22,6 +24,10 @@ struct DraftArgs {
   float* q_stats;
   void* ws;
   const void* gate = nullptr;  // gated head: gate values [V, rank] (bf16); null = Markov head
+  // a round's schedule, computed by the drafting launch itself when the tensor-core sweep runs and the
+  // problem is small (R * gamma <= 4096); *sched_done tells the caller whether it was
+  const ScheduleArgs* sched = nullptr;
+  bool* sched_done = nullptr;
 };
 
 struct ScheduleArgs {

@@ -15,29 +15,9 @@
 // Theta_i comparisons in float64 with the operation order fixed by the C ABI.
 #include "common.cuh"
 #include "internal.h"
+#include "sched_common.cuh"
 
 namespace dspark {
-
-// Coalesced copy of n words from global (L2) to shared memory with eight loads
-// in flight per thread (a load-then-store loop would wait out one memory round
-// trip per iteration).
-template <class T>
-__device__ void stage_smem(T* dst, const T* src, int n) {
-  constexpr int kU = 8;
-  for (int base = threadIdx.x; base < n; base += kU * blockDim.x) {
-    T v[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int j = base + u * blockDim.x;
-      v[u] = j < n ? __ldcg(src + j) : T();
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int j = base + u * blockDim.x;
-      if (j < n) dst[j] = v[u];
-    }
-  }
-}
 
 constexpr int kSchedThreads = 1024;
 constexpr int kDigits = 16;
@@ -76,29 +56,6 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
   const unsigned long long res = (w > 0 ? sh[w - 1] : 0ull) + ex;
   __syncthreads();
   return res;
-}
-
-// a in [0, 1] -> ascending sort key (descending a); bits of +0.0 .. 1.0.
-__device__ __forceinline__ uint32_t survival_key(float a) { return 0x3F800000u - __float_as_uint(a); }
-__device__ __forceinline__ float key_survival(uint32_t key) { return __uint_as_float(0x3F800000u - key); }
-
-// floor(a * 2^40 + 1/2) for a float32 a in [0, 1], with integer operations
-// (equal to the same expression evaluated exactly in float64).
-__device__ __forceinline__ unsigned long long fixed_point(float a) {
-  const uint32_t b = __float_as_uint(a);
-  const int e = (int)((b >> 23) & 0xFFu);
-  if (e == 0) return 0ull;  // zero or subnormal: below 2^-41
-  const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
-  const int sh = e - 110;  // a * 2^40 = m * 2^(e - 110)
-  if (sh >= 0) return m << sh;
-  const int s = -sh;
-  if (s > 40) return 0ull;
-  return (m + (1ull << (s - 1))) >> s;
-}
-
-__device__ __forceinline__ double theta_of(int R, unsigned long long S, float sps) {
-  const double tau = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
-  return __dmul_rn(tau, (double)sps);
 }
 
 // Survival keys of one confidence matrix; flags non-finite entries.
@@ -331,63 +288,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 // the prefix at K of the current order, and counts L_r = #{j : p(r, j) < K}
 // (the order is prefix-closed within a request).
 constexpr int kRankThreads = 256;
-constexpr int kRankSplit = 16;
 constexpr int kRankKeysPerCta = kRankThreads / kRankSplit;
 constexpr int kRankMaxKeys = 4096;
 // keys + fixed-point survivals, current and lagged
 constexpr size_t kSmallSmem = 2 * (size_t)kRankMaxKeys * (sizeof(uint32_t) + sizeof(unsigned long long));
-
-// The confidences are staged in `key` by one coalesced pass, then each row's
-// running product overwrites them in place; fxv receives fixed_point(a).
-__device__ void survival_keys_smem(const float* conf, int R, int gamma, uint32_t* key, unsigned long long* fxv,
-                                   uint32_t* status) {
-  const int n = R * gamma;
-  stage_smem(key, reinterpret_cast<const uint32_t*>(conf), n);
-  __syncthreads();
-  for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    float acc = 1.f;
-    for (int j = 0; j < gamma; ++j) {
-      float c = __uint_as_float(key[r * gamma + j]);
-      if (!isfinite(c)) {
-        set_status(status, DSPARK_ERR_NONFINITE);
-        c = 0.f;
-      }
-      c = c > 0.f ? fminf(c, 1.f) : 0.f;
-      acc = __fmul_rn(acc, c);
-      key[r * gamma + j] = survival_key(acc);
-      fxv[r * gamma + j] = fixed_point(acc);
-    }
-  }
-}
-
-// Sorted position of candidate i and the fixed-point sum of the survivals
-// before it; every thread of the kRankSplit-lane group that holds i gets both.
-__device__ __forceinline__ void rank_and_prefix(const uint32_t* key, const unsigned long long* fxv, int n, int i,
-                                                int s, int& pos, unsigned long long& before_sum) {
-  const uint32_t ki = key[min(i, n - 1)];
-  int cnt = 0;
-  unsigned long long sum = 0ull;
-#pragma unroll 4
-  for (int j = s; j < n; j += kRankSplit) {
-    const uint32_t kj = key[j];
-    const bool before = (kj < ki) || (kj == ki && j < i);
-    cnt += before;
-    sum += before ? fxv[j] : 0ull;
-  }
-#pragma unroll
-  for (int o = kRankSplit / 2; o > 0; o >>= 1) {
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  }
-  pos = cnt;
-  before_sum = sum;
-}
-
-// float64 bits -> unsigned key with the same order
-__device__ __forceinline__ unsigned long long ordered_bits(double x) {
-  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
-  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
-}
 
 __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
@@ -417,38 +321,39 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     if (badv) atomicOr(bad_table, 1u);
   }
 
-  survival_keys_smem(conf, R, gamma, key, fxv, status);
-  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, fxl, status);
+  auto sync_all = [] { __syncthreads(); };
+  survival_keys_smem(conf, R, gamma, key, fxv, status, tid, T, sync_all);
+  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, fxl, status, tid, T, sync_all);
   __syncthreads();
   const int i = blockIdx.x * kRankKeysPerCta + tid / kRankSplit;
   const int s = tid % kRankSplit;
   const bool mine = s == 0 && i < n;
   const bool table_ok = R <= n_table;
   if (mode == DSPARK_SCHED_ALL) {  // the sum is order-free: each CTA adds its own candidates
-    unsigned long long v = mine ? fxv[i] : 0ull;
+    unsigned long long v = mine ? cand_fx(fxv, gamma, i) : 0ull;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if ((tid & 31) == 0 && v) atomicAdd(all_sum, v);
   } else {
     int p;
     unsigned long long Sb;
-    rank_and_prefix(key, fxv, n, i, s, p, Sb);
+    rank_and_prefix(key, fxv, R, gamma, i, s, p, Sb);
     if (mine) {
       pos_g[i] = (uint32_t)p;
-      prefix_g[p] = Sb + fxv[i];  // inclusive prefix at sorted position p
+      prefix_g[p] = Sb + cand_fx(fxv, gamma, i);  // inclusive prefix at sorted position p
       if (mode == DSPARK_SCHED_CAUSAL && table_ok) {
         const int B = R + p + 1;
         bool st = B > n_table;
-        if (!st) st = theta_of(R, Sb + fxv[i], sps[B - 1]) < theta_of(R, Sb, sps[B - 2]);
+        if (!st) st = theta_of(R, Sb + cand_fx(fxv, gamma, i), sps[B - 1]) < theta_of(R, Sb, sps[B - 2]);
         if (st) atomicMax(stop_enc, (unsigned)(n - p));
       }
     }
     if (lagged) {
       int pl;
       unsigned long long Sl;
-      rank_and_prefix(keyl, fxl, n, i, s, pl, Sl);
+      rank_and_prefix(keyl, fxl, R, gamma, i, s, pl, Sl);
       if (mine && table_ok && pl + 1 <= min(n, n_table - R))  // Theta_{pl+1} of the lagged order
-        theta_lag_g[pl] = ordered_bits(theta_of(R, Sl + fxl[i], sps[R + pl]));
+        theta_lag_g[pl] = ordered_bits(theta_of(R, Sl + cand_fx(fxl, gamma, i), sps[R + pl]));
     }
   }
   __syncthreads();
