@@ -694,8 +694,8 @@ def main():
         "round_us_direct_call": None if direct_ms is None else direct_ms * 1e3,
         "round_us_p10_median_p90": [pct[10], pct[50], pct[90]],
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
-        "stages_note": ("each entry point timed alone; inside dspark_round the schedule of up to 4,096 "
-                        "candidates runs as the last phase of the drafting launch (no launch of its own)"),
+        "stages_note": ("each entry point timed alone; inside dspark_round one extra CTA of the drafting "
+                        "launch computes the schedule while the other CTAs sweep (no launch of its own)"),
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
         "gated_head": gated,

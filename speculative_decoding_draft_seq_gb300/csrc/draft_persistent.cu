@@ -105,10 +105,9 @@ struct PersistParams {
   unsigned long long* lsum;     // [R * gamma] 2^-40 sums of max(0, P - Q), zero between calls
   float* labels;                // [R, gamma]
   int label_tma;                // label pass: target and base boxes by TMA (else per-warp row copies)
-  // the round's prefix schedule, run as a last phase of the drafting launch (its inputs do not depend on
-  // the drafted tokens): the candidates' counting rank spread over every CTA, then one grid barrier
+  // the round's prefix schedule, computed by one extra CTA of the drafting launch (blockIdx.x == n_cta)
+  // while the others sweep: its inputs do not depend on the drafted tokens
   int sched_on;
-  int sched_prefetch;            // the inputs below are 16-byte aligned: prefetched into L2 at launch
   const float* conf;             // [R, gamma]
   const float* conf_lag;         // [R, gamma] (LAGGED)
   const float* sps;              // [n_table]
@@ -116,15 +115,15 @@ struct PersistParams {
   int32_t* sched_len;            // [R]
   int32_t* sched_K;              // [1]
   double* tau_theta;             // [2]
-  uint32_t* pos_g;               // [R * gamma] sorted position of each candidate
-  unsigned long long* prefix_g;  // [R * gamma] inclusive 2^-40 prefix sums by sorted position
-  unsigned long long* theta_lag_g;  // [R * gamma] ordered bits of Theta_{p+1} on the lagged order
+  uint32_t *skey0, *skey1, *sidx0, *sidx1;  // [R * gamma] sort buffers, when the keys do not fit shared memory
+  unsigned long long* sched_fx;  // [R * gamma] fixed-point prefix sums in sorted order
 };
-// The scheduling phase's counters, in the status block after the grid-barrier counter (cleared with it
-// before every launch): the stop word, the order-free sum (ALL mode) and the cost-table flag.
-constexpr int kSchedStopWord = 16, kSchedSumWord = 18, kSchedBadWord = 20;
-// Candidates the phase keeps in shared memory (keys and fixed-point survivals, current and lagged).
-constexpr int kSchedFuseMax = 4096;
+// The scheduler CTA's shared memory: radix counters for its threads, the four key / index arrays, and the
+// reduction scratch.
+constexpr uint32_t kSchedCntBytes = (uint32_t)kDigits * kPThreads * 4;
+constexpr uint32_t kSchedKeysBytes = 4u * kSmemKeys * 4;
+static_assert(kSchedCntBytes + kSchedKeysBytes + 32 * (8 + 4 + 8) + 16 <= kPSmem - 1024,
+              "the scheduler CTA's tables fit the launch's shared memory");
 
 // Per-request constants of the residual pass: P(v) = 2^((t_v - M_P) log2e/T) / Z_P
 // from the target row stats, Q(v) from the draft stats of the rejected position.
@@ -1011,6 +1010,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   volatile int* sDecide = reinterpret_cast<volatile int*>(sTmem + 2);  // epilogue-group verdict
 
+  if (!kResid && p.sched_on && blockIdx.x == (unsigned)p.n_cta) {
+    // The scheduler CTA ("Verificação com agendamento por confiança"): the whole prefix schedule with
+    // every thread of the block, concurrently with the sweep of the other CTAs (it takes part in none
+    // of their barriers).
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSchedCntBytes);
+    unsigned long long* shu = reinterpret_cast<unsigned long long*>(smem + kSchedCntBytes + kSchedKeysBytes);
+    double* shd = reinterpret_cast<double*>(shu + 32);
+    int* shi = reinterpret_cast<int*>(shd + 32);
+    const BlockSchedScratch sc{cnt, p.R * p.gamma <= kSmemKeys ? keys : nullptr, shu, shi, shd, shi + 32};
+    schedule_block(p.R, p.gamma, p.conf, p.conf_lag, p.sps, p.n_table, p.sched_mode, p.sched_len, p.sched_K,
+                   p.tau_theta, p.skey0, p.skey1, p.sidx0, p.sidx1, p.sched_fx, p.status, sc);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c_begin = (int)(((long long)blockIdx.x * p.nc) / p.n_cta);
   const int c_end = (int)(((long long)(blockIdx.x + 1) * p.nc) / p.n_cta);
@@ -1041,14 +1054,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t tmem = *sTmem;
 
   if (warp == 0) {
-    if (lane == 0 && !kResid && p.sched_on && p.sched_prefetch && blockIdx.x == 0) {
-      // the schedule's inputs into L2 now (a hint nothing waits on), so that the scheduling phase at the
-      // end of the launch finds them there: whole 16-byte units only
-      const uint32_t cb = (uint32_t)(p.R * p.gamma) * 4u & ~15u, tb = (uint32_t)p.n_table * 4u & ~15u;
-      if (cb) bulk_prefetch_l2(p.conf, cb);
-      if (cb && p.sched_mode == DSPARK_SCHED_LAGGED) bulk_prefetch_l2(p.conf_lag, cb);
-      if (tb) bulk_prefetch_l2(p.sps, tb);
-    }
     if (lane == 0) {  // W2 producer: streams across steps, ahead of the tokens
       prefetch_tensormap(&mapW2);
       const uint64_t pol = l2_policy_evict_last();
@@ -1445,137 +1450,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (*sDecide) break;
       }
     }
-    if (!kResid && p.sched_on && !stop) {
-      // The round's prefix schedule ("Verificação com agendamento por confiança"), every CTA: the
-      // copies and MMAs of the sweep are over, so the A region and the W2 ring hold the survival keys
-      // and fixed-point survivals (current and lagged). CTA b ranks candidates 16 b .. 16 b + 15, then
-      // 16 (b + n_cta) .., sixteen threads per candidate; a grid barrier; then every CTA counts the
-      // lengths of its requests and CTA 0 writes K and (tau, Theta).
-      const int n = p.R * p.gamma;
-      const int mode = p.sched_mode;
-      const bool lagged = mode == DSPARK_SCHED_LAGGED, table_ok = p.R <= p.n_table;
-      uint32_t* key = reinterpret_cast<uint32_t*>(sA);
-      unsigned long long* fxv = reinterpret_cast<unsigned long long*>(sA + 4 * kSchedFuseMax);
-      uint32_t* keyl = reinterpret_cast<uint32_t*>(sB);
-      unsigned long long* fxl = reinterpret_cast<unsigned long long*>(sB + 4 * kSchedFuseMax);
-      unsigned int* stop_enc = p.status + kSchedStopWord;
-      unsigned long long* all_sum = reinterpret_cast<unsigned long long*>(p.status + kSchedSumWord);
-      unsigned int* bad_table = p.status + kSchedBadWord;
-      {  // this CTA's slice of the cost table must be finite
-        const int per = ceil_div(p.n_table, p.n_cta);
-        const int j0 = (int)blockIdx.x * per, j1 = min(j0 + per, p.n_table);
-        bool badv = false;
-        for (int j = j0 + et; j < j1; j += kPEpiThreads) badv |= !isfinite(__ldg(p.sps + j));
-        if (badv) atomicOr(bad_table, 1u);
-      }
-      auto sync_group = [] { eg_sync(); };
-      survival_keys_smem(p.conf, p.R, p.gamma, key, fxv, p.status, et, kPEpiThreads, sync_group);
-      if (lagged) survival_keys_smem(p.conf_lag, p.R, p.gamma, keyl, fxl, p.status, et, kPEpiThreads, sync_group);
-      eg_sync();
-      constexpr int kPerPass = kPEpiThreads / kRankSplit;
-      for (int b0 = (int)blockIdx.x * kPerPass; b0 < n; b0 += p.n_cta * kPerPass) {  // CTA-uniform
-        const int i = b0 + et / kRankSplit, s = et % kRankSplit;
-        const bool mine = s == 0 && i < n;
-        if (mode == DSPARK_SCHED_ALL) {  // order-free: each CTA adds its own candidates
-          unsigned long long v = mine ? cand_fx(fxv, p.gamma, i) : 0ull;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0 && v) atomicAdd(all_sum, v);
-          continue;
-        }
-        int pp;
-        unsigned long long Sb;
-        rank_and_prefix(key, fxv, p.R, p.gamma, i, s, pp, Sb);
-        if (mine) {
-          p.pos_g[i] = (uint32_t)pp;
-          p.prefix_g[pp] = Sb + cand_fx(fxv, p.gamma, i);  // inclusive prefix at sorted position pp
-          if (mode == DSPARK_SCHED_CAUSAL && table_ok) {
-            const int B = p.R + pp + 1;
-            bool st = B > p.n_table;
-            if (!st) st = theta_of(p.R, Sb + cand_fx(fxv, p.gamma, i), p.sps[B - 1]) < theta_of(p.R, Sb, p.sps[B - 2]);
-            if (st) atomicMax(stop_enc, (unsigned)(n - pp));
-          }
-        }
-        if (lagged) {
-          int pl;
-          unsigned long long Sl;
-          rank_and_prefix(keyl, fxl, p.R, p.gamma, i, s, pl, Sl);
-          if (mine && table_ok && pl + 1 <= min(n, p.n_table - p.R))  // Theta_{pl+1} of the lagged order
-            p.theta_lag_g[pl] = ordered_bits(theta_of(p.R, Sl + cand_fx(fxl, p.gamma, i), p.sps[p.R + pl]));
-        }
-      }
-      eg_sync();
-      if (et == 0) {  // every CTA's ranks are in
-        ++epoch;
-        *sDecide = (*sAbort || !grid_barrier(p.gbar, epoch * (unsigned)p.n_cta, p.status, sAbort)) ? 1 : 0;
-      }
-      eg_sync();
-      if (*sDecide) {
-        stop = true;
-      } else {
-        const unsigned int enc = __ldcg(stop_enc), bad = __ldcg(bad_table);
-        int K = 0;
-        unsigned long long S = 0ull;
-        float sps_K = 0.f;
-        bool by_K = false;  // lengths from the first K sorted positions
-        if (bad) {
-          if (blockIdx.x == 0 && et == 0) set_status(p.status, DSPARK_ERR_NONFINITE);
-        } else if (mode == DSPARK_SCHED_ALL) {
-          K = n;
-          S = __ldcg(all_sum);
-          sps_K = p.R + n <= p.n_table ? p.sps[p.R + n - 1] : 0.f;
-        } else if (table_ok) {
-          by_K = true;
-          if (lagged) {  // smallest argmax of Theta_i, i = 0..imax (Theta_0 = Theta(R, 0)), every CTA
-            const int imax = min(n, p.n_table - p.R);
-            unsigned long long best = 0ull;
-            int besti = 0x7fffffff;
-            for (int j = et; j <= imax; j += kPEpiThreads) {
-              const unsigned long long th =
-                  j == 0 ? ordered_bits(theta_of(p.R, 0ull, p.sps[p.R - 1])) : __ldcg(p.theta_lag_g + (j - 1));
-              if (th > best || (th == best && j < besti)) { best = th; besti = j; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
-              const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-              if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
-            }
-            unsigned long long* sBest = reinterpret_cast<unsigned long long*>(sA);  // keys are no longer read
-            int* sBestI = reinterpret_cast<int*>(sA + 64);
-            eg_sync();
-            if (lane == 0) { sBest[ew] = best; sBestI[ew] = besti; }
-            eg_sync();
-            best = 0ull;
-            besti = 0x7fffffff;
-            for (int w = 0; w < kPEpiWarps; ++w)
-              if (sBest[w] > best || (sBest[w] == best && sBestI[w] < besti)) { best = sBest[w]; besti = sBestI[w]; }
-            K = besti;
-          } else {
-            K = enc ? n - (int)enc : n;
-          }
-          if (K > 0) S = __ldcg(p.prefix_g + (K - 1));
-          sps_K = p.sps[p.R + K - 1];
-        }
-        // L_r = #{j : pos(r, j) < K} (the order is prefix-closed within a request); request r by CTA
-        // r mod n_cta, warp (r / n_cta) mod 8
-        for (int r = blockIdx.x + ew * p.n_cta; r < p.R; r += kPEpiWarps * p.n_cta) {
-          int c = 0;
-          if (by_K)
-            for (int j = lane; j < p.gamma; j += 32) c += __ldcg(p.pos_g + (size_t)r * p.gamma + j) < (uint32_t)K;
-          else if (!bad && mode == DSPARK_SCHED_ALL)
-            c = lane == 0 ? p.gamma : 0;
-          c = warp_sum_i(c);
-          if (lane == 0) p.sched_len[r] = c;
-        }
-        if (blockIdx.x == 0 && et == 0) {
-          *p.sched_K = K;
-          p.tau_theta[0] = __dadd_rn((double)p.R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
-          p.tau_theta[1] = (by_K || (mode == DSPARK_SCHED_ALL && !bad && p.R + n <= p.n_table))
-                               ? theta_of(p.R, S, sps_K) : 0.0;
-        }
-      }
-    }
     if (kResid) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
     if (et == 0 && a_phases > 0)  // nor an A box the MMA issuer stopped waiting for
       for (int ka = 0; ka < 4; ++ka) mbar_wait_drain(&aFull[ka], (a_phases - 1) & 1, p.status);
@@ -1649,7 +1523,11 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   PersistParams p{};
   p.R = a.R; p.gamma = a.gamma; p.V = a.V; p.rank = a.rank;
   p.nc = ceil_div(a.V, kChunk);
-  p.n_cta = p.nc < sms ? p.nc : sms;
+  // with a schedule, one CTA slot is the scheduler's: the sweep takes the others
+  const int slots = sms * per_sm;
+  const bool sched = a.sched != nullptr && slots >= 2;
+  const int sweep_slots = sched ? slots - 1 : slots;
+  p.n_cta = p.nc < sweep_slots ? p.nc : sweep_slots;
   p.n_mt = ceil_div(a.R, kPM);
   p.box_rows = box_rows;
   p.greedy = a.temperature == 0.f;
@@ -1668,8 +1546,7 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   p.astage = ws_at<__nv_bfloat16>(a.ws, L.astage);
   p.gate = static_cast<const __nv_bfloat16*>(a.gate);
   p.gcarry = ws_at<float>(a.ws, L.gcarry);
-  const bool sched = a.sched && (long long)a.R * a.gamma <= kSchedFuseMax;
-  if (sched) {  // the round's schedule as the launch's last phase
+  if (sched) {  // the round's schedule, by the launch's extra CTA
     const ScheduleArgs& sa = *a.sched;
     p.sched_on = 1;
     p.conf = sa.conf;
@@ -1680,20 +1557,18 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
     p.sched_len = sa.sched_len;
     p.sched_K = sa.K;
     p.tau_theta = sa.tau_theta;
-    p.pos_g = ws_at<uint32_t>(a.ws, L.skey0);
-    p.prefix_g = ws_at<unsigned long long>(a.ws, L.fx);
-    p.theta_lag_g = ws_at<unsigned long long>(a.ws, L.fx2);
-    p.sched_prefetch = ((reinterpret_cast<uintptr_t>(sa.conf) | reinterpret_cast<uintptr_t>(sa.sps) |
-                         (sa.mode == DSPARK_SCHED_LAGGED ? reinterpret_cast<uintptr_t>(sa.conf_lagged) : 0)) & 15) == 0;
+    p.skey0 = ws_at<uint32_t>(a.ws, L.skey0);
+    p.skey1 = ws_at<uint32_t>(a.ws, L.skey1);
+    p.sidx0 = ws_at<uint32_t>(a.ws, L.sidx0);
+    p.sidx1 = ws_at<uint32_t>(a.ws, L.sidx1);
+    p.sched_fx = ws_at<unsigned long long>(a.ws, L.fx);
   }
   taken = true;
-  // the grid-barrier counter (and with a schedule, its counters up to word kSchedBadWord) start at zero
-  cudaError_t e = cudaMemsetAsync(p.gbar, 0, (sched ? kSchedBadWord : 1) * sizeof(unsigned int), s);
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);  // the grid-barrier counter
   if (e != cudaSuccess) return e;
   if (sched && a.sched_done) *a.sched_done = true;
   void* args[] = {&mapW2, &mapBase, &mapA, &mapW2, &p};  // no target map in this mode
-  e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kPThreads), args,
-                                  kPSmem, s);
+  e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta + (sched ? 1 : 0)), dim3(kPThreads), args, kPSmem, s);
   launches += 1;
   return e;
 }

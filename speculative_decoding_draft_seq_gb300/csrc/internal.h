@@ -24,8 +24,8 @@ struct DraftArgs {
   float* q_stats;
   void* ws;
   const void* gate = nullptr;  // gated head: gate values [V, rank] (bf16); null = Markov head
-  // a round's schedule, computed by the drafting launch itself when the tensor-core sweep runs and the
-  // problem is small (R * gamma <= 4096); *sched_done tells the caller whether it was
+  // a round's schedule, computed by one extra CTA of the drafting launch when the tensor-core sweep
+  // runs; *sched_done tells the caller whether it was
   const ScheduleArgs* sched = nullptr;
   bool* sched_done = nullptr;
 };

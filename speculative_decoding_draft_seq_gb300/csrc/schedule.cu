@@ -17,127 +17,13 @@
 #include "internal.h"
 #include "sched_common.cuh"
 
+#include <algorithm>
+
 namespace dspark {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kDigits = 16;
-// Up to this many candidates the sort keys and indices live in shared memory.
-constexpr int kSmemKeys = 8192;
-constexpr size_t kCntBytes = (size_t)kDigits * kSchedThreads * sizeof(uint32_t);
-constexpr size_t kSchedSmemMax = kCntBytes + 4 * (size_t)kSmemKeys * sizeof(uint32_t);
-
-// Exclusive scan of one unsigned 64-bit value per thread; returns the total.
-__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v,
-                                                               unsigned long long* sh,
-                                                               unsigned long long& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  unsigned long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  unsigned long long ex = __shfl_up_sync(0xffffffffu, x, 1);
-  if (lane == 0) ex = 0;
-  __syncthreads();
-  if (lane == 31) sh[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    unsigned long long s = lane < nw ? sh[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nw) sh[lane] = s;
-  }
-  __syncthreads();
-  total = sh[nw - 1];
-  const unsigned long long res = (w > 0 ? sh[w - 1] : 0ull) + ex;
-  __syncthreads();
-  return res;
-}
-
-// Survival keys of one confidence matrix; flags non-finite entries.
-// `stage` (n words) receives the confidences in one coalesced pass first.
-__device__ void build_keys(const float* conf, int R, int gamma, uint32_t* key, uint32_t* idx,
-                           uint32_t* stage, uint32_t* status) {
-  const int n = R * gamma;
-  stage_smem(stage, reinterpret_cast<const uint32_t*>(conf), n);
-  __syncthreads();
-  for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    float acc = 1.f;
-    for (int j = 0; j < gamma; ++j) {
-      float c = __uint_as_float(stage[(size_t)r * gamma + j]);
-      if (!isfinite(c)) {
-        set_status(status, DSPARK_ERR_NONFINITE);
-        c = 0.f;
-      }
-      c = c > 0.f ? fminf(c, 1.f) : 0.f;
-      acc = __fmul_rn(acc, c);
-      key[(size_t)r * gamma + j] = survival_key(acc);
-      idx[(size_t)r * gamma + j] = (uint32_t)(r * gamma + j);
-    }
-  }
-  __syncthreads();
-}
-
-// Stable LSD radix sort of (key, idx), 8 passes of 4 bits; result in key0/idx0.
-__device__ void radix_sort(uint32_t* key0, uint32_t* idx0, uint32_t* key1, uint32_t* idx1, int n,
-                           uint32_t* cnt, unsigned long long* shu) {
-  const int T = blockDim.x, tid = threadIdx.x;
-  const int seg = ceil_div(n, T);
-  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-  uint32_t *kin = key0, *iin = idx0, *kout = key1, *iout = idx1;
-  for (int shift = 0; shift < 32; shift += 4) {
-    for (int d = 0; d < kDigits; ++d) cnt[d * T + tid] = 0;
-    for (int i = s0; i < s1; ++i) cnt[((kin[i] >> shift) & 15u) * T + tid] += 1;
-    __syncthreads();
-    uint32_t loc[kDigits];
-    unsigned long long sum = 0;
-#pragma unroll
-    for (int j = 0; j < kDigits; ++j) {
-      loc[j] = cnt[kDigits * tid + j];
-      sum += loc[j];
-    }
-    unsigned long long tot;
-    unsigned long long run = block_exscan_u64(sum, shu, tot);
-#pragma unroll
-    for (int j = 0; j < kDigits; ++j) {
-      cnt[kDigits * tid + j] = (uint32_t)run;
-      run += loc[j];
-    }
-    __syncthreads();
-    for (int i = s0; i < s1; ++i) {
-      const uint32_t k = kin[i];
-      const uint32_t slot = ((k >> shift) & 15u) * T + tid;
-      const uint32_t pos = cnt[slot];
-      cnt[slot] = pos + 1;
-      kout[pos] = k;
-      iout[pos] = iin[i];
-    }
-    __syncthreads();
-    uint32_t* t;
-    t = kin; kin = kout; kout = t;
-    t = iin; iin = iout; iout = t;
-  }
-}
-
-// fx[i] = sum of fixed_point(a) over sorted positions 0..i.
-__device__ void fixed_prefix(const uint32_t* key, int n, unsigned long long* fx, unsigned long long* shu) {
-  const int T = blockDim.x, tid = threadIdx.x;
-  const int seg = ceil_div(n, T);
-  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-  unsigned long long loc = 0;
-  for (int i = s0; i < s1; ++i) loc += fixed_point(key_survival(key[i]));
-  unsigned long long tot;
-  unsigned long long run = block_exscan_u64(loc, shu, tot);
-  for (int i = s0; i < s1; ++i) {
-    run += fixed_point(key_survival(key[i]));
-    fx[i] = run;
-  }
-  __syncthreads();
-}
+constexpr size_t kSchedSmemMax = (size_t)kDigits * kSchedThreads * sizeof(uint32_t) +
+                                  4 * (size_t)kSmemKeys * sizeof(uint32_t);
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
@@ -149,149 +35,62 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   __shared__ int shi[32];
   __shared__ double shd[32];
   __shared__ int sBad;
-  const int tid = threadIdx.x, T = blockDim.x;
-  const int n = R * gamma;
-  if (n <= kSmemKeys) {  // sort in shared memory
-    uint32_t* sk = cnt + kDigits * kSchedThreads;
-    key0 = sk;
-    key1 = sk + kSmemKeys;
-    idx0 = sk + 2 * kSmemKeys;
-    idx1 = sk + 3 * kSmemKeys;
-  }
-
-  if (tid == 0) sBad = 0;
-  __syncthreads();
-  for (int i = tid; i < n_table; i += T)
-    if (!isfinite(sps[i])) sBad = 1;
-  for (int r = tid; r < R; r += T) L[r] = (mode == DSPARK_SCHED_ALL) ? gamma : 0;
-  __syncthreads();
-  if (sBad) {
-    if (tid == 0) {
-      set_status(status, DSPARK_ERR_NONFINITE);
-      *Kout = 0;
-      tau_theta[0] = (double)R;
-      tau_theta[1] = 0.0;
-    }
-    for (int r = tid; r < R; r += T) L[r] = 0;
-    return;
-  }
-
-  if (mode == DSPARK_SCHED_ALL) {
-    build_keys(conf, R, gamma, key0, idx0, key1, status);
-    unsigned long long loc = 0;
-    for (int i = tid; i < n; i += T) loc += fixed_point(key_survival(key0[i]));
-    unsigned long long tot;
-    block_exscan_u64(loc, shu, tot);
-    if (tid == 0) {
-      *Kout = n;
-      tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(tot), 0x1p-40));
-      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, tot, sps[R + n - 1]) : 0.0;
-    }
-    return;
-  }
-
-  if (R > n_table) {
-    if (tid == 0) {
-      *Kout = 0;
-      tau_theta[0] = (double)R;
-      tau_theta[1] = 0.0;
-    }
-    return;
-  }
-
-  int K = 0;
-  if (mode == DSPARK_SCHED_LAGGED) {
-    build_keys(conf_lag, R, gamma, key0, idx0, key1, status);
-    radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
-    fixed_prefix(key0, n, fx, shu);
-    const int imax = min(n, n_table - R);
-    // smallest argmax of Theta_i, i = 0..imax
-    double best = -INFINITY;
-    int besti = 0x7fffffff;
-    for (int i = tid; i <= imax; i += T) {
-      const unsigned long long S = i ? fx[i - 1] : 0ull;
-      const double th = theta_of(R, S, sps[R + i - 1]);
-      if (th > best || (th == best && i < besti)) { best = th; besti = i; }
-    }
-    // block (value, index) argmax in float64
-    const int lane = tid & 31, w = tid >> 5, nw = T >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-      if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
-    }
-    __syncthreads();
-    if (lane == 0) { shd[w] = best; shi[w] = besti; }
-    __syncthreads();
-    best = lane < nw ? shd[lane] : -INFINITY;
-    besti = lane < nw ? shi[lane] : 0x7fffffff;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-      if (ob > best || (ob == best && oi < besti)) { best = ob; besti = oi; }
-    }
-    K = besti;
-    __syncthreads();
-  }
-
-  build_keys(conf, R, gamma, key0, idx0, key1, status);
-  radix_sort(key0, idx0, key1, idx1, n, cnt, shu);
-  fixed_prefix(key0, n, fx, shu);
-
-  if (mode == DSPARK_SCHED_CAUSAL) {
-    const int seg = ceil_div(n, T);
-    const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-    int stop = 0x7fffffff;
-    for (int i = s0; i < s1; ++i) {
-      const int B = R + i + 1;
-      bool st = B > n_table;
-      if (!st) {
-        const double th_next = theta_of(R, fx[i], sps[B - 1]);
-        const double th_prev = theta_of(R, i ? fx[i - 1] : 0ull, sps[B - 2]);
-        st = th_next < th_prev;
-      }
-      if (st) { stop = i; break; }
-    }
-    K = block_min_i(stop, shi);
-    if (K == 0x7fffffff) K = n;
-  }
-
-  for (int i = tid; i < K; i += T) atomicAdd(&L[idx0[i] / (uint32_t)gamma], 1);
-  if (tid == 0) {
-    const unsigned long long S = K ? fx[K - 1] : 0ull;
-    *Kout = K;
-    tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(S), 0x1p-40));
-    tau_theta[1] = theta_of(R, S, sps[R + K - 1]);
-  }
+  const BlockSchedScratch sc{cnt, R * gamma <= kSmemKeys ? cnt + kDigits * blockDim.x : nullptr, shu, shi, shd,
+                             &sBad};
+  schedule_block(R, gamma, conf, conf_lag, sps, n_table, mode, L, Kout, tau_theta, key0, key1, idx0, idx1, fx,
+                 status, sc);
 }
 
 // ---------------------------------------------------------------------------
-// Small problems (R * gamma <= kRankMaxKeys): one launch of many CTAs instead
-// of one CTA.
+// Small problems (R * gamma <= kRankMaxKeys): one launch of up to one CTA per
+// SM instead of one CTA.
 //
-// Every CTA forms all the survival keys and their fixed-point values in
-// shared memory. For each of its own kRankKeysPerCta candidates, kRankSplit
-// threads count over interleaved slices of the keys both the candidates
-// before it in the ascending key order (ties by flat index: the radix sort's
-// order) and the fixed-point sum of their survivals. So the CTA knows the
-// candidate's sorted position p and the exact prefix sums S_p (before it) and
-// S_p + f (with it), and evaluates the admission rule at that position:
+// Every CTA forms all the survival keys and their running fixed-point row
+// sums in shared memory (column-major tables, conflict-free for a warp). Warp
+// w of CTA b takes candidates 8 b + w, 8 (b + grid) + w, ...: its 32 lanes
+// count over the rows both the candidates before it in the ascending key
+// order (ties by flat index: the radix sort's order) and the fixed-point sum
+// of their survivals. So the warp knows the candidate's sorted position p and
+// the exact prefix sums S_p (before it) and S_p + f (with it), and evaluates
+// the admission rule at that position:
 //   CAUSAL: admitting position p stops the scheduler iff B = R + p + 1 >
 //     n_table or Theta(S_p + f, SPS[B - 1]) < Theta(S_p, SPS[B - 2]); the
 //     smallest stopping position is K, gathered by an atomic max of n - p;
 //   LAGGED: Theta_{p+1} on the lagged order, written for the argmax;
-//   ALL: the survivals' sum, gathered by an atomic add.
+//   ALL: nothing (every candidate is admitted; the sum of all survivals is
+//     the sum of the rows' last running sums).
 // The last CTA to finish (a counter in the status block; it resets every
 // counter it used) reads K (LAGGED: the smallest argmax of the Theta_i),
 // the prefix at K of the current order, and counts L_r = #{j : p(r, j) < K}
 // (the order is prefix-closed within a request).
 constexpr int kRankThreads = 256;
-constexpr int kRankKeysPerCta = kRankThreads / kRankSplit;
+constexpr int kRankWarps = kRankThreads / 32;
 constexpr int kRankMaxKeys = 4096;
-// keys + fixed-point survivals, current and lagged
-constexpr size_t kSmallSmem = 2 * (size_t)kRankMaxKeys * (sizeof(uint32_t) + sizeof(unsigned long long));
+constexpr int kRankStageMax = kRankMaxKeys * 3 / 2;  // R (gamma | 1) <= 3/2 R gamma
+
+// Byte offsets of the tables in dynamic shared memory (the lagged ones empty
+// unless LAGGED), and their total.
+struct SmallLayout {
+  int Rs, m;
+  size_t fxv, fxl, key, keyl, stg, stgl, spsv, bytes;
+};
+inline __host__ __device__ SmallLayout small_layout(int R, int gamma, int n_table, bool lagged) {
+  SmallLayout L;
+  L.Rs = sched_col_stride(R, gamma, kRankMaxKeys);
+  L.m = sched_sps_count(R, gamma, n_table);
+  const size_t T = (size_t)L.Rs * gamma, S = (size_t)R * sched_stage_stride(gamma), nl = lagged ? 1 : 0;
+  L.fxv = 0;
+  L.fxl = L.fxv + 8 * T;
+  L.key = L.fxl + nl * 8 * T;
+  L.keyl = L.key + 4 * T;
+  L.stg = L.keyl + nl * 4 * T;
+  L.stgl = L.stg + 4 * S;
+  L.spsv = L.stgl + nl * 4 * S;
+  L.bytes = L.spsv + 4 * (size_t)L.m;
+  return L;
+}
+constexpr size_t kSmallSmemMax =
+    2 * (size_t)kRankMaxKeys * 12 + 2 * 4 * (size_t)kRankStageMax + 4 * ((size_t)kRankMaxKeys + 1);
 
 __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     int R, int gamma, const float* __restrict__ conf, const float* __restrict__ conf_lag,
@@ -299,61 +98,61 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     unsigned long long* theta_lag_g, int32_t* __restrict__ L, int32_t* __restrict__ Kout,
     double* __restrict__ tau_theta, uint32_t* status) {
   extern __shared__ __align__(16) unsigned char sm_raw[];
-  unsigned long long* fxv = reinterpret_cast<unsigned long long*>(sm_raw);
-  unsigned long long* fxl = fxv + kRankMaxKeys;
-  uint32_t* key = reinterpret_cast<uint32_t*>(fxl + kRankMaxKeys);
-  uint32_t* keyl = key + kRankMaxKeys;
+  const bool lagged = mode == DSPARK_SCHED_LAGGED;
+  const SmallLayout Ly = small_layout(R, gamma, n_table, lagged);
+  unsigned long long* fxv = reinterpret_cast<unsigned long long*>(sm_raw + Ly.fxv);
+  unsigned long long* fxl = reinterpret_cast<unsigned long long*>(sm_raw + Ly.fxl);
+  uint32_t* key = reinterpret_cast<uint32_t*>(sm_raw + Ly.key);
+  uint32_t* keyl = reinterpret_cast<uint32_t*>(sm_raw + Ly.keyl);
+  uint32_t* stg = reinterpret_cast<uint32_t*>(sm_raw + Ly.stg);
+  uint32_t* stgl = reinterpret_cast<uint32_t*>(sm_raw + Ly.stgl);
+  const float* spsv = reinterpret_cast<const float*>(sm_raw + Ly.spsv);
   __shared__ int sLast;
-  __shared__ unsigned long long sMax[kRankThreads / 32];
-  __shared__ int sMaxI[kRankThreads / 32];
+  __shared__ unsigned long long sMax[kRankWarps];
+  __shared__ int sMaxI[kRankWarps];
   unsigned int* done = status + 2;
-  unsigned long long* all_sum = reinterpret_cast<unsigned long long*>(status + 4);
   unsigned int* stop_enc = status + 6;
   unsigned int* bad_table = status + 8;
-  const int tid = threadIdx.x, T = blockDim.x;
-  const int n = R * gamma;
-  const bool lagged = mode == DSPARK_SCHED_LAGGED;
-  {  // this CTA's slice of the cost table must be finite
+  const int tid = threadIdx.x, T = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int n = R * gamma, Rs = Ly.Rs;
+  bool badv = false;
+  {  // this CTA's slice of the cost table must be finite (loads in flight with the staging's)
     const int per = ceil_div(n_table, (int)gridDim.x);
     const int j0 = (int)blockIdx.x * per, j1 = min(j0 + per, n_table);
-    bool badv = false;
     for (int j = j0 + tid; j < j1; j += T) badv |= !isfinite(__ldg(sps + j));
-    if (badv) atomicOr(bad_table, 1u);
   }
-
-  auto sync_all = [] { __syncthreads(); };
-  survival_keys_smem(conf, R, gamma, key, fxv, status, tid, T, sync_all);
-  if (lagged) survival_keys_smem(conf_lag, R, gamma, keyl, fxl, status, tid, T, sync_all);
+  stage_sched_inputs(conf, lagged ? conf_lag : nullptr, sps, R, gamma, Ly.m, stg, stgl,
+                     reinterpret_cast<float*>(sm_raw + Ly.spsv), tid, T);
+  if (badv) atomicOr(bad_table, 1u);
   __syncthreads();
-  const int i = blockIdx.x * kRankKeysPerCta + tid / kRankSplit;
-  const int s = tid % kRankSplit;
-  const bool mine = s == 0 && i < n;
+  survival_tables(stg, R, gamma, Rs, key, fxv, status, tid, T);
+  if (lagged) survival_tables(stgl, R, gamma, Rs, keyl, fxl, status, tid, T);
+  __syncthreads();
   const bool table_ok = R <= n_table;
-  if (mode == DSPARK_SCHED_ALL) {  // the sum is order-free: each CTA adds its own candidates
-    unsigned long long v = mine ? cand_fx(fxv, gamma, i) : 0ull;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((tid & 31) == 0 && v) atomicAdd(all_sum, v);
-  } else {
-    int p;
-    unsigned long long Sb;
-    rank_and_prefix(key, fxv, R, gamma, i, s, p, Sb);
-    if (mine) {
-      pos_g[i] = (uint32_t)p;
-      prefix_g[p] = Sb + cand_fx(fxv, gamma, i);  // inclusive prefix at sorted position p
-      if (mode == DSPARK_SCHED_CAUSAL && table_ok) {
-        const int B = R + p + 1;
-        bool st = B > n_table;
-        if (!st) st = theta_of(R, Sb + cand_fx(fxv, gamma, i), sps[B - 1]) < theta_of(R, Sb, sps[B - 2]);
-        if (st) atomicMax(stop_enc, (unsigned)(n - p));
+  if (mode != DSPARK_SCHED_ALL) {
+    for (int i = (int)blockIdx.x * kRankWarps + warp; i < n; i += (int)gridDim.x * kRankWarps) {  // warp-uniform
+      const int r = i / gamma, j = i - r * gamma;
+      int p;
+      unsigned long long Sb;
+      rank_and_prefix(key, fxv, R, gamma, Rs, r, j, lane, p, Sb);
+      if (lane == 0) {
+        const unsigned long long f = cand_fx(fxv, Rs, r, j);
+        pos_g[i] = (uint32_t)p;
+        prefix_g[p] = Sb + f;  // inclusive prefix at sorted position p
+        if (mode == DSPARK_SCHED_CAUSAL && table_ok) {  // SPS(B) = spsv[B - R]
+          const int B = R + p + 1;
+          bool st = B > n_table;
+          if (!st) st = theta_of(R, Sb + f, spsv[p + 1]) < theta_of(R, Sb, spsv[p]);
+          if (st) atomicMax(stop_enc, (unsigned)(n - p));
+        }
       }
-    }
-    if (lagged) {
-      int pl;
-      unsigned long long Sl;
-      rank_and_prefix(keyl, fxl, R, gamma, i, s, pl, Sl);
-      if (mine && table_ok && pl + 1 <= min(n, n_table - R))  // Theta_{pl+1} of the lagged order
-        theta_lag_g[pl] = ordered_bits(theta_of(R, Sl + cand_fx(fxl, gamma, i), sps[R + pl]));
+      if (lagged) {
+        int pl;
+        unsigned long long Sl;
+        rank_and_prefix(keyl, fxl, R, gamma, Rs, r, j, lane, pl, Sl);
+        if (lane == 0 && table_ok && pl + 1 <= min(n, n_table - R))  // Theta_{pl+1} of the lagged order
+          theta_lag_g[pl] = ordered_bits(theta_of(R, Sl + cand_fx(fxl, Rs, r, j), spsv[pl + 1]));
+      }
     }
   }
   __syncthreads();
@@ -366,13 +165,11 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   __threadfence();
 
   // admission (last CTA)
-  const unsigned long long total = __ldcg(all_sum);
   const unsigned int enc = __ldcg(stop_enc);
   const unsigned int bad = __ldcg(bad_table);
   __syncthreads();
   if (tid == 0) {  // every counter back to zero for the next call
     *done = 0u;
-    *all_sum = 0ull;
     *stop_enc = 0u;
     *bad_table = 0u;
   }
@@ -387,11 +184,12 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     return;
   }
   if (mode == DSPARK_SCHED_ALL) {
+    const unsigned long long total = survival_total(fxv, R, gamma, Rs, sMax, tid, T, [] { __syncthreads(); });
     for (int r = tid; r < R; r += T) L[r] = gamma;
     if (tid == 0) {
       *Kout = n;
       tau_theta[0] = __dadd_rn((double)R, __dmul_rn(__ull2double_rn(total), 0x1p-40));
-      tau_theta[1] = (R + n >= 1 && R + n <= n_table) ? theta_of(R, total, sps[R + n - 1]) : 0.0;
+      tau_theta[1] = R + n <= n_table ? theta_of(R, total, spsv[n]) : 0.0;
     }
     return;
   }
@@ -411,7 +209,7 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
     int besti = 0x7fffffff;
     for (int j = tid; j <= imax; j += T) {
       const unsigned long long th =
-          j == 0 ? ordered_bits(theta_of(R, 0ull, sps[R - 1])) : __ldcg(theta_lag_g + (j - 1));
+          j == 0 ? ordered_bits(theta_of(R, 0ull, spsv[0])) : __ldcg(theta_lag_g + (j - 1));
       if (th > best || (th == best && j < besti)) { best = th; besti = j; }
     }
 #pragma unroll
@@ -435,7 +233,7 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
   float sps_K = 0.f;
   if (tid == 0) {
     S = K ? __ldcg(prefix_g + (K - 1)) : 0ull;
-    sps_K = __ldg(sps + R + K - 1);
+    sps_K = spsv[K];  // SPS(R + K)
   }
   uint32_t* srank = key;  // the positions, staged over the key array
   stage_smem(srank, pos_g, n);
@@ -455,27 +253,31 @@ __global__ void __launch_bounds__(kRankThreads) schedule_small_kernel(
 // Both scheduler forms behind one call: the many-CTA rank kernel (admission
 // in its last CTA) for small problems, the single-CTA radix sort otherwise.
 // Scratch: key0/key1/idx0/idx1 (u32[n] each), fx (u64[n]), for the small form
-// fx2 (u64[n]); status[0] is the sticky status word, status[2], [4..5], [6]
-// and [8] the small form's completion counter, sum, stop word and cost-table
-// flag (zero between calls).
+// fx2 (u64[n]); status[0] is the sticky status word, status[2], [6] and [8]
+// the small form's completion counter, stop word and cost-table flag (zero
+// between calls).
 cudaError_t schedule_launch(const ScheduleArgs& a, uint32_t* key0, uint32_t* key1, uint32_t* idx0, uint32_t* idx1,
                             unsigned long long* fx, unsigned long long* fx2, uint32_t* status, cudaStream_t s,
                             int& launches) {
   const long long n = (long long)a.R * a.gamma;
   if (n <= kRankMaxKeys) {
-    const int grid = (int)ceil_div(n, kRankKeysPerCta);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // at most one CTA per SM: every CTA builds the whole tables
+    const int grid = std::min(ceil_div(n, kRankWarps), std::max(sms, 1));
+    const size_t smem = small_layout(a.R, a.gamma, a.n_table, a.mode == DSPARK_SCHED_LAGGED).bytes;
     static std::atomic<unsigned long long> attr{0};
-    {
-      cudaError_t e = set_smem_limit_once((const void*)schedule_small_kernel, (int)kSmallSmem, attr);
-      if (e != cudaSuccess) return e;
-    }
-    schedule_small_kernel<<<grid, kRankThreads, kSmallSmem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps,
-                                                                 a.n_table, a.mode, key0, fx, fx2, a.sched_len, a.K,
-                                                                 a.tau_theta, status);
+    e = set_smem_limit_once((const void*)schedule_small_kernel, (int)kSmallSmemMax, attr);
+    if (e != cudaSuccess) return e;
+    schedule_small_kernel<<<grid, kRankThreads, smem, s>>>(a.R, a.gamma, a.conf, a.conf_lagged, a.sps, a.n_table,
+                                                           a.mode, key0, fx, fx2, a.sched_len, a.K, a.tau_theta,
+                                                           status);
     launches += 1;
     return cudaGetLastError();
   }
-  const size_t smem = kCntBytes + (n <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
+  const size_t smem = (size_t)kDigits * kSchedThreads * 4 + (n <= kSmemKeys ? 4 * (size_t)kSmemKeys * 4 : 0);
   static std::atomic<unsigned long long> attr{0};
   {
     cudaError_t e = set_smem_limit_once((const void*)schedule_kernel, (int)kSchedSmemMax, attr);

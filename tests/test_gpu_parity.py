@@ -257,8 +257,8 @@ def test_tensor_core_path_shapes(R, gamma, V, rank, T):
                      conf_law="decreasing", table="concave", n_table=R * (gamma + 1))
     rep, g, _ = _full(cfg)
     assert rep["positions"] > 0
-    # one persistent drafting launch that ends with the round's schedule, the row stats, and (sampled)
-    # the residual sweep: the tensor-core path, not the CUDA-core kernels
+    # one persistent drafting launch (one of its CTAs computes the round's schedule), the row stats, and
+    # (sampled) the residual sweep: the tensor-core path, not the CUDA-core kernels
     assert g["launches"] == (3 if T > 0 else 2), g["launches"]
 
 
@@ -276,8 +276,9 @@ def test_many_requests(gated):
     g = gpu_round(cfg)
     rep = compare(cfg, g, oracle_pool.oracle_round(cfg, requests, chunk=64), requests)
     assert rep["resid_compared"] > 0 and rep["bonus_compared"] > 0, rep
-    # draft, scheduler, row statistics with chains, (gated) state staging, residual sweep
-    assert g["launches"] == (5 if gated else 4), g["launches"]
+    # draft (its extra CTA schedules the 16,400 candidates), row statistics with chains, (gated) state
+    # staging, residual sweep
+    assert g["launches"] == (4 if gated else 3), g["launches"]
 
 
 @pytest.mark.parametrize("cfg", [RAGGED_FP32, W.with_(RAGGED_BF16, mode=W.LAGGED, conf_law="beta_mixed"),
