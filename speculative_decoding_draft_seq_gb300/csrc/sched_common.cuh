@@ -275,25 +275,42 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
   return res;
 }
 
+// The one-block scheduler's sequential loops over a thread's segment read
+// kBatch elements ahead of the dependent work: when the arrays live in the
+// workspace (global memory, generic pointers the compiler cannot separate
+// from the shared counters) each batch costs one memory round trip instead
+// of one per element.
+constexpr int kBatch = 8;
+
 // Survival keys of one confidence matrix; flags non-finite entries.
 // `stage` (n words) receives the confidences in one coalesced pass first.
 inline __device__ void build_keys(const float* conf, int R, int gamma, uint32_t* key, uint32_t* idx,
-                           uint32_t* stage, uint32_t* status) {
+                                  uint32_t* stage, uint32_t* status) {
   const int n = R * gamma;
   stage_smem(stage, reinterpret_cast<const uint32_t*>(conf), n);
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     float acc = 1.f;
-    for (int j = 0; j < gamma; ++j) {
-      float c = __uint_as_float(stage[(size_t)r * gamma + j]);
-      if (!isfinite(c)) {
-        set_status(status, DSPARK_ERR_NONFINITE);
-        c = 0.f;
+    const size_t row = (size_t)r * gamma;
+    for (int j0 = 0; j0 < gamma; j0 += kBatch) {
+      uint32_t cb[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) cb[u] = j0 + u < gamma ? stage[row + j0 + u] : 0u;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u;
+        if (j < gamma) {
+          float c = __uint_as_float(cb[u]);
+          if (!isfinite(c)) {
+            set_status(status, DSPARK_ERR_NONFINITE);
+            c = 0.f;
+          }
+          c = c > 0.f ? fminf(c, 1.f) : 0.f;
+          acc = __fmul_rn(acc, c);
+          key[row + j] = survival_key(acc);
+          idx[row + j] = (uint32_t)(row + j);
+        }
       }
-      c = c > 0.f ? fminf(c, 1.f) : 0.f;
-      acc = __fmul_rn(acc, c);
-      key[(size_t)r * gamma + j] = survival_key(acc);
-      idx[(size_t)r * gamma + j] = (uint32_t)(r * gamma + j);
     }
   }
   __syncthreads();
@@ -301,14 +318,21 @@ inline __device__ void build_keys(const float* conf, int R, int gamma, uint32_t*
 
 // Stable LSD radix sort of (key, idx), 8 passes of 4 bits; result in key0/idx0.
 inline __device__ void radix_sort(uint32_t* key0, uint32_t* idx0, uint32_t* key1, uint32_t* idx1, int n,
-                           uint32_t* cnt, unsigned long long* shu) {
+                                  uint32_t* cnt, unsigned long long* shu) {
   const int T = blockDim.x, tid = threadIdx.x;
   const int seg = ceil_div(n, T);
   const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
   uint32_t *kin = key0, *iin = idx0, *kout = key1, *iout = idx1;
   for (int shift = 0; shift < 32; shift += 4) {
     for (int d = 0; d < kDigits; ++d) cnt[d * T + tid] = 0;
-    for (int i = s0; i < s1; ++i) cnt[((kin[i] >> shift) & 15u) * T + tid] += 1;
+    for (int i0 = s0; i0 < s1; i0 += kBatch) {
+      uint32_t kb[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) kb[u] = i0 + u < s1 ? kin[i0 + u] : 0u;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (i0 + u < s1) cnt[((kb[u] >> shift) & 15u) * T + tid] += 1;
+    }
     __syncthreads();
     uint32_t loc[kDigits];
     unsigned long long sum = 0;
@@ -325,13 +349,23 @@ inline __device__ void radix_sort(uint32_t* key0, uint32_t* idx0, uint32_t* key1
       run += loc[j];
     }
     __syncthreads();
-    for (int i = s0; i < s1; ++i) {
-      const uint32_t k = kin[i];
-      const uint32_t slot = ((k >> shift) & 15u) * T + tid;
-      const uint32_t pos = cnt[slot];
-      cnt[slot] = pos + 1;
-      kout[pos] = k;
-      iout[pos] = iin[i];
+    for (int i0 = s0; i0 < s1; i0 += kBatch) {
+      uint32_t kb[kBatch], ib[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        kb[u] = i0 + u < s1 ? kin[i0 + u] : 0u;
+        ib[u] = i0 + u < s1 ? iin[i0 + u] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (i0 + u < s1) {
+          const uint32_t slot = ((kb[u] >> shift) & 15u) * T + tid;
+          const uint32_t pos = cnt[slot];
+          cnt[slot] = pos + 1;
+          kout[pos] = kb[u];
+          iout[pos] = ib[u];
+        }
+      }
     }
     __syncthreads();
     uint32_t* t;
@@ -347,12 +381,24 @@ inline __device__ void fixed_prefix(const uint32_t* key, int n, unsigned long lo
   const int seg = ceil_div(n, T);
   const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
   unsigned long long loc = 0;
-  for (int i = s0; i < s1; ++i) loc += fixed_point(key_survival(key[i]));
+  for (int i0 = s0; i0 < s1; i0 += kBatch) {
+    uint32_t kb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) kb[u] = i0 + u < s1 ? key[i0 + u] : 0x3F800000u;  // survival 0
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) loc += fixed_point(key_survival(kb[u]));
+  }
   unsigned long long tot;
   unsigned long long run = block_exscan_u64(loc, shu, tot);
-  for (int i = s0; i < s1; ++i) {
-    run += fixed_point(key_survival(key[i]));
-    fx[i] = run;
+  for (int i0 = s0; i0 < s1; i0 += kBatch) {
+    uint32_t kb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) kb[u] = i0 + u < s1 ? key[i0 + u] : 0x3F800000u;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      run += fixed_point(key_survival(kb[u]));
+      if (i0 + u < s1) fx[i0 + u] = run;
+    }
   }
   __syncthreads();
 }
@@ -479,15 +525,25 @@ inline __device__ void schedule_block(int R, int gamma, const float* __restrict_
     const int seg = ceil_div(n, T);
     const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
     int stop = 0x7fffffff;
-    for (int i = s0; i < s1; ++i) {
-      const int B = R + i + 1;
-      bool st = B > n_table;
-      if (!st) {
-        const double th_next = theta_of(R, fx[i], sps[B - 1]);
-        const double th_prev = theta_of(R, i ? fx[i - 1] : 0ull, sps[B - 2]);
-        st = th_next < th_prev;
+    for (int i0 = s0; i0 < s1 && stop == 0x7fffffff; i0 += kBatch) {
+      // prefix sums S_{i0-1} .. S_{i0+kBatch-1} and SPS(R + i0) .. SPS(R + i0 + kBatch), read together
+      unsigned long long fb[kBatch + 1];
+      float tb[kBatch + 1];
+#pragma unroll
+      for (int u = 0; u <= kBatch; ++u) {
+        const int i = i0 + u - 1, B = R + i + 1;  // fb[u] = S_i, tb[u] = SPS[B - 1]
+        fb[u] = (i >= 0 && i < s1) ? fx[i] : 0ull;
+        tb[u] = (i < s1 && B >= 1 && B <= n_table) ? sps[B - 1] : 0.f;
       }
-      if (st) { stop = i; break; }
+#pragma unroll
+      for (int u = 1; u <= kBatch; ++u) {
+        const int i = i0 + u - 1, B = R + i + 1;
+        if (i < s1 && stop == 0x7fffffff) {
+          bool st = B > n_table;
+          if (!st) st = theta_of(R, fb[u], tb[u]) < theta_of(R, fb[u - 1], tb[u - 1]);
+          if (st) stop = i;
+        }
+      }
     }
     K = block_min_i(stop, shi);
     if (K == 0x7fffffff) K = n;
