@@ -213,12 +213,18 @@ static dspark_status round_entry(int32_t R, int32_t gamma, int32_t V, int32_t ra
     return DSPARK_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int n = 0;
-  // the schedule's inputs do not depend on the draft: the tensor-core drafting launch computes it as its
-  // last phase when the problem is small, else the scheduler runs as its own launch
+  // The schedule's inputs do not depend on the draft, nor do the target row statistics that verification
+  // needs (given the schedule): on the tensor-core path the drafting launch computes both while it sweeps,
+  // and runs the acceptance chains after its last draw; else the scheduler and verification run as their
+  // own launches. In ALL mode every target row is verified, more than the launch's spare CTAs can stream
+  // during the sweep, and verification keeps its own launch.
   ScheduleArgs sa{R, gamma, conf, conf_lagged, sps_table, n_table, mode, sched_len, K, tau_theta, workspace};
-  bool sched_done = false;
+  VerifyArgs va{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens,
+                q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace, gate};
+  bool sched_done = false, verify_done = false;
   DraftArgs da{R, gamma, V, rank, dtype, base_logits, anchor, W1, W2, temperature, seed,
-               draft_tokens, q_tok, q_stats, workspace, gate, &sa, &sched_done};
+               draft_tokens, q_tok, q_stats, workspace, gate, &sa, &sched_done,
+               mode == DSPARK_SCHED_ALL ? nullptr : &va, &verify_done};
   cudaError_t e;
   if (gate) {
     bool taken = false;
@@ -228,11 +234,7 @@ static dspark_status round_entry(int32_t R, int32_t gamma, int32_t V, int32_t ra
     e = launch_draft(da, s, n);
   }
   if (e == cudaSuccess && !sched_done) e = launch_schedule(sa, s, n);
-  if (e == cudaSuccess) {
-    VerifyArgs va{R, gamma, V, rank, dtype, target_logits, base_logits, anchor, W1, W2, draft_tokens,
-                  q_tok, q_stats, sched_len, temperature, seed, out_tokens, accepted_len, p_tok, workspace, gate};
-    e = launch_verify(va, s, n);
-  }
+  if (e == cudaSuccess) e = verify_done ? launch_verify_tail(va, s, n) : launch_verify(va, s, n);
   g_last_launches = n;
   return cuda_status(e);
 }

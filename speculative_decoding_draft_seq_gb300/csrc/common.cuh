@@ -20,6 +20,8 @@ inline __host__ __device__ size_t align256(size_t x) { return (x + 255) & ~(size
 
 // Pieces each target row is split into by the row-stats pass (one CTA each).
 constexpr int kVsSplit = 4;
+// Pieces per target row in the drafting launch's row statistics (a warp each).
+constexpr int kVsPieceMax = 8;
 
 // Per-request pending draw of the verifier (residual or bonus).
 enum PendKind : int { kPendNone = 0, kPendResid = 1, kPendBonus = 2 };
@@ -33,7 +35,8 @@ struct WsLayout {
   size_t rpart;    // float2 [R][n_chunks]   residual chunk partials (sum res, sum P)
   size_t astage;   // bf16   [2][R][rank]    W1 rows of the drafted tokens, by step parity (rank <= 256)
   size_t gcarry;   // float  [R][256]        gated head: float32 state of each request between steps
-  size_t vsplit;   // float4 [R][gamma+1][kVsSplit] target row piece stats (M_s, Z_s, max, argmax)
+  size_t vsplit;   // float4 [R][gamma+1][kVsPieceMax] target row piece stats (M_s, Z_s, max, argmax)
+  size_t vlist;    // u32    [R*(gamma+1)]   the scheduled target rows, listed by the drafting launch
   size_t vcount;   // u32    [R*(gamma+1) + R] row / request completion counters (zero between calls)
   size_t lstage;   // bf16   [R*gamma][256]  acceptance labels: W1 rows of every (request, position)
   size_t lsum;     // u64    [R*gamma]       acceptance labels: 2^-40 sums of max(0, P - Q) (zero between calls)
@@ -58,7 +61,8 @@ inline __host__ __device__ WsLayout ws_layout(int R, int gamma, int V) {
   L.pend = o;    o = align256(o + (size_t)R * sizeof(int4));
   L.astage = o;  o = align256(o + (size_t)2 * R * 256 * 2);
   L.gcarry = o;  o = align256(o + (size_t)R * 256 * sizeof(float));
-  L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * kVsSplit * sizeof(float4));
+  L.vsplit = o;  o = align256(o + (size_t)R * (gamma + 1) * kVsPieceMax * sizeof(float4));
+  L.vlist = o;   o = align256(o + (size_t)R * (gamma + 1) * sizeof(uint32_t));
   L.lstage = o;  o = align256(o + (size_t)R * gamma * 256 * 2);
   L.lsum = o;    o = align256(o + (size_t)R * gamma * sizeof(unsigned long long));
   L.skey0 = o;   o = align256(o + n * sizeof(uint32_t));

@@ -28,7 +28,10 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sched_common.cuh"
+#include "verify_common.cuh"
 #include "tc_ptx.cuh"
+
+#include <algorithm>
 
 namespace dspark {
 
@@ -94,10 +97,11 @@ struct PersistParams {
   const __nv_bfloat16* gate;  // [V, rank] gate values in [0, 1]; null for the Markov head
   float* gcarry;              // [R][256] float32 state s_k of each request between steps
   uint32_t* status;
-  // residual / bonus pass of verification
+  // residual / bonus pass of verification (target, rowstat, pend and out_tokens also serve the drafting
+  // launch's verification work below)
   const __nv_bfloat16* target;  // [R, gamma+1, V]
-  const int4* pend;             // (kind, target row A, prev token, A)
-  const float4* rowstat;        // target row stats (M, Z, argmax, -)
+  int4* pend;                   // (kind, target row A, prev token, A)
+  float4* rowstat;              // target row stats (M, Z, argmax, -)
   int32_t* out_tokens;          // [R, gamma+1]
   float2* rpart;                // [R][nc] (sum max(0, P - Q), sum P)
   // acceptance labels (one pass over every (request, position) pair)
@@ -117,13 +121,36 @@ struct PersistParams {
   double* tau_theta;             // [2]
   uint32_t *skey0, *skey1, *sidx0, *sidx1;  // [R * gamma] sort buffers, when the keys do not fit shared memory
   unsigned long long* sched_fx;  // [R * gamma] fixed-point prefix sums in sorted order
+  // verification's row statistics and chains in the same launch: the scheduler CTA lists the scheduled
+  // target rows; the CTAs past it stream their statistics while the sweep runs; after its last draw each
+  // sweep CTA takes the rows still queued, then runs the chains of its requests
+  int vfuse;
+  float4* vpieces;               // [R (gamma + 1)][kVwSplit]
+  unsigned int* row_cnt;         // [R (gamma + 1)] (zero between calls)
+  unsigned int* req_cnt;         // [R] (zero between calls)
+  uint32_t* vlist;               // [R (gamma + 1)]
+  float* p_tok;                  // [R, gamma]
+  int32_t* accepted_len;         // [R]
+  int stage_rank;                // rank when the chain stages the residual pass's A rows (Markov head), else 0
 };
+// Status words of the launch's verification work (cleared with the grid-barrier counter before the
+// launch): the scheduled-row count plus one once the list is published, and the work queue's head.
+constexpr int kVReadyWord = 16, kVQueueWord = 17;
+// Row-statistics CTAs at most (the CTAs past the scheduler's).
+constexpr int kRowCtasMax = 16;
+
 // The scheduler CTA's shared memory: radix counters for its threads, the four key / index arrays, and the
 // reduction scratch.
 constexpr uint32_t kSchedCntBytes = (uint32_t)kDigits * kPThreads * 4;
 constexpr uint32_t kSchedKeysBytes = 4u * kSmemKeys * 4;
 static_assert(kSchedCntBytes + kSchedKeysBytes + 32 * (8 + 4 + 8) + 16 <= kPSmem - 1024,
               "the scheduler CTA's tables fit the launch's shared memory");
+static_assert(kPWarps * (kVwRingBytes + 8 * kVwSlots) <= kPSmem - 1024,
+              "a row-statistics CTA's rings and their mbarriers fit the launch's shared memory");
+static_assert(kPEpiWarps * kVwRingBytes <= kPBStages * kPBStage + 2 * kPBaseStages * kPBaseBox &&
+                  kOddOffset + kPEpiWarps * kVwSlots * 8 <= 1024,
+              "after the sweep, the epilogue warps' rings fit the W2 and base rings, their mbarriers the uniforms "
+              "table");
 
 // Per-request constants of the residual pass: P(v) = 2^((t_v - M_P) log2e/T) / Z_P
 // from the target row stats, Q(v) from the draft stats of the rejected position.
@@ -250,6 +277,94 @@ __device__ bool grid_barrier(unsigned int* counter, unsigned int target, uint32_
   atomicCAS(status, 0u, (uint32_t)DSPARK_ERR_TIMEOUT);
   *abort = 1;
   return false;
+}
+
+// Bounded acquire poll of a counter another CTA of the launch advances: true
+// once it reaches `target`; on timeout records DSPARK_ERR_TIMEOUT and returns
+// false. One thread calls it.
+__device__ bool wait_count(const unsigned int* word, unsigned int target, uint32_t* status) {
+  for (uint32_t i = 0; i < kGridSpinLimit; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+    if (v >= target) return true;
+    if (i > 16) __nanosleep(128);
+  }
+  atomicCAS(status, 0u, (uint32_t)DSPARK_ERR_TIMEOUT);
+  return false;
+}
+
+// The scheduled target rows r (gamma + 1) + k, k <= L_r, listed request by
+// request, by every thread of the scheduler CTA after the schedule is
+// written; then the count plus one is published (release) in the ready word.
+__device__ void list_scheduled_rows(const PersistParams& p, unsigned long long* shu) {
+  __syncthreads();
+  unsigned long long run = 0ull;
+  for (int b = 0; b < p.R; b += (int)blockDim.x) {  // block-uniform
+    const int r = b + (int)threadIdx.x;
+    const int c = r < p.R ? min(max(__ldcg(p.sched_len + r), 0), p.gamma) + 1 : 0;
+    unsigned long long tot;
+    const unsigned long long ex = block_exscan_u64((unsigned long long)c, shu, tot);
+    for (int k = 0; k < c; ++k) p.vlist[run + ex + k] = (uint32_t)(r * (p.gamma + 1) + k);
+    run += tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int v = (unsigned int)run + 1u;
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.status + kVReadyWord), "r"(v) : "memory");
+  }
+}
+
+// A warp's row-statistics setup: initialises its ring's kVwSlots mbarriers
+// (`rbars`) and waits for the row list. False on timeout.
+__device__ bool row_work_setup(const PersistParams& p, int lane, uint64_t* rbars, RowWork& w) {
+  if (lane == 0) {
+    for (int i = 0; i < kVwSlots; ++i) mbar_init(rbars + i, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  unsigned int ready = 0u;
+  if (lane == 0) ready = wait_count(p.status + kVReadyWord, 1u, p.status) ? __ldcg(p.status + kVReadyWord) : 0u;
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  __syncwarp();
+  w = RowWork{p.target, p.vlist, (int)(ready ? ready - 1u : 0u) * kVwSplit, p.vpieces, p.row_cnt, p.req_cnt,
+              p.rowstat, p.status + kVQueueWord, p.gamma, p.V, p.greedy, p.kT};
+  return ready != 0u;
+}
+
+// A row-statistics CTA's warp: pieces from the queue one at a time until it
+// is empty, streamed through `ring` (kVwRingBytes of shared memory).
+__device__ bool row_stats_warp(const PersistParams& p, int lane, unsigned char* ring, uint64_t* rbars) {
+  RowWork w;
+  if (!row_work_setup(p, lane, rbars, w)) return false;
+  return row_items_warp(w, lane, ring, rbars, p.status);
+}
+
+// The eight epilogue warps of a sweep CTA after its last draw: one atomic
+// claims eight pieces (one per warp) at a time, so that the CTAs that reach
+// the queue together do not all queue on its counter. Every warp takes part
+// in every round's two named barriers, a warp whose wait ran out included;
+// warp 0's view of the queue decides for all (sClaim: two words). False if
+// the row list never came or a wait ran out.
+__device__ bool row_stats_cta(const PersistParams& p, int ew, int lane, unsigned char* ring, uint64_t* rbars,
+                              volatile unsigned int* sClaim) {
+  RowWork w;
+  bool ok = row_work_setup(p, lane, rbars, w);
+  const uint64_t policy = l2_policy_evict_first();
+  uint32_t n_issued = 0u, n_done = 0u;
+  for (;;) {  // sClaim[0] = the round's first item, sClaim[1] = the item count, both from warp 0's view
+    if (ew == 0 && lane == 0) {
+      sClaim[0] = ok ? atomicAdd(w.queue, (unsigned int)kPEpiWarps) : 0u;
+      sClaim[1] = ok ? (unsigned int)w.n_items : 0u;
+    }
+    eg_sync();
+    const unsigned int base = sClaim[0], n_items = sClaim[1];
+    eg_sync();
+    if (base >= n_items) break;  // CTA-uniform
+    const unsigned int item = base + (unsigned int)ew;
+    if (ok && item < n_items) ok = row_item(w, item, lane, ring, rbars, n_issued, n_done, policy, p.status);
+  }
+  return ok;
 }
 
 }  // namespace dspark
@@ -1010,18 +1125,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   volatile int* sDecide = reinterpret_cast<volatile int*>(sTmem + 2);  // epilogue-group verdict
 
-  if (!kResid && p.sched_on && blockIdx.x == (unsigned)p.n_cta) {
-    // The scheduler CTA ("Verificação com agendamento por confiança"): the whole prefix schedule with
-    // every thread of the block, concurrently with the sweep of the other CTAs (it takes part in none
-    // of their barriers).
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSchedCntBytes);
-    unsigned long long* shu = reinterpret_cast<unsigned long long*>(smem + kSchedCntBytes + kSchedKeysBytes);
-    double* shd = reinterpret_cast<double*>(shu + 32);
-    int* shi = reinterpret_cast<int*>(shd + 32);
-    const BlockSchedScratch sc{cnt, p.R * p.gamma <= kSmemKeys ? keys : nullptr, shu, shi, shd, shi + 32};
-    schedule_block(p.R, p.gamma, p.conf, p.conf_lag, p.sps, p.n_table, p.sched_mode, p.sched_len, p.sched_K,
-                   p.tau_theta, p.skey0, p.skey1, p.sidx0, p.sidx1, p.sched_fx, p.status, sc);
+  if (!kResid && p.sched_on && blockIdx.x >= (unsigned)p.n_cta) {
+    // The CTAs past the sweep's, concurrently with it (they take part in none of its barriers). CTA n_cta
+    // is the scheduler ("Verificação com agendamento por confiança"): the whole prefix schedule with every
+    // thread of the block, then the list of the target rows verification reads. With verification in the
+    // launch, it and the CTAs after it then stream those rows' statistics, one piece per warp.
+    if (blockIdx.x == (unsigned)p.n_cta) {
+      uint32_t* cnt = reinterpret_cast<uint32_t*>(smem);
+      uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSchedCntBytes);
+      unsigned long long* shu = reinterpret_cast<unsigned long long*>(smem + kSchedCntBytes + kSchedKeysBytes);
+      double* shd = reinterpret_cast<double*>(shu + 32);
+      int* shi = reinterpret_cast<int*>(shd + 32);
+      const BlockSchedScratch sc{cnt, p.R * p.gamma <= kSmemKeys ? keys : nullptr, shu, shi, shd, shi + 32};
+      schedule_block(p.R, p.gamma, p.conf, p.conf_lag, p.sps, p.n_table, p.sched_mode, p.sched_len, p.sched_K,
+                     p.tau_theta, p.skey0, p.skey1, p.sidx0, p.sidx1, p.sched_fx, p.status, sc);
+      if (p.vfuse) list_scheduled_rows(p, shu);
+    }
+    if (p.vfuse) {  // every warp streams pieces through its own ring; the mbarriers follow the rings
+      const int w = (int)(threadIdx.x >> 5);
+      row_stats_warp(p, (int)(threadIdx.x & 31), smem + (size_t)w * kVwRingBytes,
+                     reinterpret_cast<uint64_t*>(smem + (size_t)kPWarps * kVwRingBytes) + w * kVwSlots);
+    }
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1450,6 +1574,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (*sDecide) break;
       }
     }
+    // the rows still queued: epilogue warp ew's ring is the ew-th 16 KB of the W2 and base rings (their copies
+    // have all landed: every stage was consumed), its mbarriers in the uniforms table (read by the draws only).
+    // The test is the group's verdict of the last barrier, the same for every warp (a warp's own `stop` is
+    // not: the work below has named barriers).
+    if (!kResid && p.vfuse && !*sDecide &&
+        row_stats_cta(p, ew, lane, sB + (size_t)ew * kVwRingBytes,
+                      reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(bars) + kOddOffset) +
+                          ew * kVwSlots,
+                      reinterpret_cast<volatile unsigned int*>(reinterpret_cast<unsigned char*>(bars) + kDepOffset))) {
+      // every CTA has drawn its last tokens (the step loop ended at a grid barrier): each warp runs the
+      // verification chain of requests blockIdx.x + ew n_cta, blockIdx.x + (ew + 8) n_cta, ... once
+      // their rows are combined
+      for (int r = (int)blockIdx.x + ew * p.n_cta; r < p.R; r += kPEpiWarps * p.n_cta) {
+        const int L = min(max(__ldcg(p.sched_len + r), 0), p.gamma);
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_count(p.req_cnt + r, (unsigned int)(L + 1), p.status) ? 1 : 0;
+          if (ok) p.req_cnt[r] = 0u;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (!ok) break;
+        request_chain(r, p.gamma, p.V, p.target, p.tokens, p.anchor, p.q_tok, p.kT, p.greedy, p.seed, p.rowstat,
+                      p.p_tok, p.out_tokens, p.accepted_len, p.pend, p.status, p.W1, p.stage_rank, p.astage, L,
+                      lane);
+      }
+    }
     if (kResid) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
     if (et == 0 && a_phases > 0)  // nor an A box the MMA issuer stopped waiting for
       for (int ka = 0; ka < 4; ++ka) mbar_wait_drain(&aFull[ka], (a_phases - 1) & 1, p.status);
@@ -1528,6 +1679,16 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
   const bool sched = a.sched != nullptr && slots >= 2;
   const int sweep_slots = sched ? slots - 1 : slots;
   p.n_cta = p.nc < sweep_slots ? p.nc : sweep_slots;
+  // with verification in the launch, the sweep keeps the fewest CTAs that leave its largest shares (chunks
+  // and requests per CTA) as they are, and up to kRowCtasMax of the slots left stream row statistics
+  const bool vfuse = sched && a.verify != nullptr && (reinterpret_cast<uintptr_t>(a.verify->target) & 15) == 0;
+  int n_row_ctas = 0;
+  if (vfuse) {
+    const int per_c = ceil_div(p.nc, p.n_cta), per_r = ceil_div(a.R, p.n_cta);
+    const int need = std::max(ceil_div(p.nc, per_c), ceil_div(a.R, per_r));
+    p.n_cta = std::min(p.n_cta, need);
+    n_row_ctas = std::min(slots - 1 - p.n_cta, kRowCtasMax);
+  }
   p.n_mt = ceil_div(a.R, kPM);
   p.box_rows = box_rows;
   p.greedy = a.temperature == 0.f;
@@ -1563,12 +1724,30 @@ cudaError_t launch_draft_persistent(const DraftArgs& a, cudaStream_t s, int& lau
     p.sidx1 = ws_at<uint32_t>(a.ws, L.sidx1);
     p.sched_fx = ws_at<unsigned long long>(a.ws, L.fx);
   }
+  if (vfuse) {
+    const VerifyArgs& va = *a.verify;
+    p.vfuse = 1;
+    p.target = static_cast<const __nv_bfloat16*>(va.target);
+    p.rowstat = ws_at<float4>(a.ws, L.rowstat);
+    p.vpieces = ws_at<float4>(a.ws, L.vsplit);
+    p.row_cnt = ws_at<unsigned int>(a.ws, L.vcount);
+    p.req_cnt = p.row_cnt + (size_t)a.R * (a.gamma + 1);
+    p.vlist = ws_at<uint32_t>(a.ws, L.vlist);
+    p.p_tok = va.p_tok;
+    p.out_tokens = va.out_tokens;
+    p.accepted_len = va.accepted_len;
+    p.pend = ws_at<int4>(a.ws, L.pend);
+    p.stage_rank = a.gate ? 0 : a.rank;  // the gated head's A rows are staged after the launch
+  }
   taken = true;
-  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned int), s);  // the grid-barrier counter
+  // the grid-barrier counter, and with verification in the launch its ready and queue words
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, (vfuse ? kVQueueWord : 1) * sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   if (sched && a.sched_done) *a.sched_done = true;
+  if (vfuse && a.verify_done) *a.verify_done = true;
   void* args[] = {&mapW2, &mapBase, &mapA, &mapW2, &p};  // no target map in this mode
-  e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta + (sched ? 1 : 0)), dim3(kPThreads), args, kPSmem, s);
+  e = cudaLaunchCooperativeKernel(fn, dim3(p.n_cta + (sched ? 1 : 0) + n_row_ctas), dim3(kPThreads), args, kPSmem,
+                                  s);
   launches += 1;
   return e;
 }

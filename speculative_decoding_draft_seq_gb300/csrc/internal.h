@@ -10,6 +10,7 @@
 namespace dspark {
 
 struct ScheduleArgs;
+struct VerifyArgs;
 
 struct DraftArgs {
   int R, gamma, V, rank, dtype;
@@ -28,6 +29,10 @@ struct DraftArgs {
   // runs; *sched_done tells the caller whether it was
   const ScheduleArgs* sched = nullptr;
   bool* sched_done = nullptr;
+  // with a schedule, the round's verification up to the residual draw (target row statistics of the
+  // scheduled rows, the acceptance chains) in the same launch; *verify_done tells whether it was
+  const VerifyArgs* verify = nullptr;
+  bool* verify_done = nullptr;
 };
 
 struct ScheduleArgs {
@@ -98,6 +103,9 @@ cudaError_t launch_draft(const DraftArgs& a, cudaStream_t s, int& launches);
 bool gated_supported(const DraftArgs& a);
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, int& launches);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches);
+// Verification after the acceptance chains (the residual / bonus draw and, for the gated head, its A
+// rows), for a round whose drafting launch computed the row statistics and chains.
+cudaError_t launch_verify_tail(const VerifyArgs& a, cudaStream_t s, int& launches);
 // Acceptance labels; `supported` is false (and nothing is launched) when the
 // sampled-mode shape is outside the tensor-core path.
 cudaError_t launch_labels(const LabelArgs& a, cudaStream_t s, int& launches, bool& supported);

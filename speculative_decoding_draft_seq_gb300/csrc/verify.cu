@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "verify_common.cuh"
 #include "internal.h"
 
 namespace dspark {
@@ -93,64 +94,6 @@ struct OnlineStat {
 // finds the first rejection, and the accepted tokens, the pending residual or
 // bonus draw, and the zeroed p of unscheduled positions are written.
 constexpr int kVsThreads = 256;
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Streaming row statistics of 8 consecutive bf16 values (one 16-byte load):
-// sampled mode keeps (max m, sum of 2^(t kT - m kT)) with a running rescale,
-// greedy mode keeps (max, lowest index of the max).
-struct RowStat {
-  float m = -INFINITY, s = 0.f;
-  int ai = 0x7fffffff;
-  __device__ __forceinline__ void add8_sampled(const uint4& q, float kT) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    float t[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      t[2 * e] = __uint_as_float(w[e] << 16);
-      t[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
-    const float gm = fmaxf(max3(t[0], t[1], t[2]), max3(t[3], t[4], max3(t[5], t[6], t[7])));
-    if (gm > m) {
-      s = m == -INFINITY ? 0.f : __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, gm), kT)));
-      m = gm;
-    }
-    const float mk = __fmul_rn(m, kT);
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      a0 += ex2_approx(__fmaf_rn(t[i], kT, -mk));
-      a1 += ex2_approx(__fmaf_rn(t[i + 1], kT, -mk));
-    }
-    s += a0 + a1;
-  }
-  __device__ __forceinline__ void add8_greedy(const uint4& q, int v0) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    float t[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      t[2 * e] = __uint_as_float(w[e] << 16);
-      t[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
-    const float gm = fmaxf(max3(t[0], t[1], t[2]), max3(t[3], t[4], max3(t[5], t[6], t[7])));
-    if (gm > m) {  // strict: the first index of a tie across groups stays
-      m = gm;
-      int i = 7;
-#pragma unroll
-      for (int j = 6; j >= 0; --j) i = t[j] == gm ? j : i;
-      ai = v0 + i;
-    }
-  }
-};
 
 // One work item: quarter sp of target row k (<= L) of request r.
 template <class Tin>
@@ -349,6 +292,44 @@ __global__ void __launch_bounds__(kVsThreads) verify_rows_kernel(
   verify_row_item<Tin>(R, gamma, V, target, tokens, anchor, q_tok, kT, greedy, seed, vsplit, row_cnt, req_cnt,
                        rowstat, p_tok, out, acc_len, pend, status, W1, rank, astage, stats_only, r, k, sp, L, shf,
                        shi, shu, sLast);
+}
+
+// bf16 target rows with V % 8 == 0, 16-byte aligned: one CTA of kVwSplit
+// warps per scheduled row (grid (R, gamma + 1), the low k first), warp w
+// streaming piece w, thread 0 combining the pieces; the CTA that combines a
+// request's last row runs the request's chain. The pieces, their combination
+// and the chain are those of the drafting launch's verification work
+// (verify_common.cuh), so both give the same bits.
+__global__ void __launch_bounds__(32 * kVwSplit) verify_rows_warp_kernel(
+    int R, int gamma, int V, const __nv_bfloat16* __restrict__ target, const int32_t* tokens,
+    const int32_t* __restrict__ anchor, const float* __restrict__ q_tok, const int32_t* __restrict__ sched_len,
+    float kT, int greedy, uint64_t seed, unsigned int* req_cnt, float4* rowstat, float* p_tok,
+    int32_t* __restrict__ out, int32_t* __restrict__ acc_len, int4* __restrict__ pend, uint32_t* status,
+    const __nv_bfloat16* __restrict__ W1, int stage_rank, __nv_bfloat16* astage) {
+  __shared__ float4 sPiece[kVwSplit];
+  __shared__ int sLast;
+  const int r = blockIdx.x, k = blockIdx.y;
+  const int L = min(max(sched_len[r], 0), gamma);
+  if (k > L) return;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t rowi = (size_t)r * (gamma + 1) + k;
+  const float4 part = warp_row_piece(target, rowi, V, w, kT, greedy, lane);
+  if (lane == 0) sPiece[w] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float4 q[kVwSplit];
+#pragma unroll
+    for (int i = 0; i < kVwSplit; ++i) q[i] = sPiece[i];
+    __stcg(rowstat + rowi, combine_row_pieces(q, kT, greedy));
+    __threadfence();
+    sLast = atomicAdd(req_cnt + r, 1u) == (unsigned)L;  // rows 0..L of this request are combined
+  }
+  __syncthreads();
+  if (!sLast || threadIdx.x >= 32) return;
+  __threadfence();
+  if (lane == 0) req_cnt[r] = 0u;
+  request_chain(r, gamma, V, target, tokens, anchor, q_tok, kT, greedy, seed, rowstat, p_tok, out, acc_len, pend,
+                status, W1, stage_rank, astage, L, lane);
 }
 
 // Residual (or bonus) weight of one entry, with explicit rounding so the
@@ -567,52 +548,70 @@ __global__ void __launch_bounds__(256) gated_stage_kernel(int R, int gamma, int 
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The residual / bonus draw (and, for the gated head, its A rows) once the
+// chains have run.
 template <class Tin>
-static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& launches) {
+static cudaError_t launch_verify_tail_t(const VerifyArgs& a, cudaStream_t s, int& launches) {
+  if (a.temperature == 0.f) return cudaGetLastError();  // greedy: the chain emitted the tokens
   const WsLayout L = ws_layout(a.R, a.gamma, a.V);
   void* ws = a.ws;
-  uint32_t* status = ws_at<uint32_t>(ws, L.status);
-  float4* rowstat = ws_at<float4>(ws, L.rowstat);
-  int4* pend = ws_at<int4>(ws, L.pend);
-  float2* rpart = ws_at<float2>(ws, L.rpart);
-  const int greedy = a.temperature == 0.f;
-  const float kT = greedy ? 0.f : (float)(1.4426950408889634 / (double)a.temperature);
+  const float kT = (float)(1.4426950408889634 / (double)a.temperature);
+  if (a.gate) {
+    gated_stage_kernel<<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, a.anchor, a.tokens,
+                                           static_cast<const __nv_bfloat16*>(a.W1),
+                                           static_cast<const __nv_bfloat16*>(a.gate), ws_at<int4>(ws, L.pend),
+                                           ws_at<__nv_bfloat16>(ws, L.astage));
+    launches += 1;
+  }
+  bool taken = false;
+  cudaError_t e = launch_resid_persistent(a, s, launches, taken);
+  if (taken || e != cudaSuccess) return e == cudaSuccess ? cudaGetLastError() : e;
+  // the fallback kernels below recompute the Markov bias; the gated head
+  // was admitted only where the tensor-core pass runs
+  if (a.gate) return cudaErrorNotSupported;
+  const int nc = ceil_div(a.V, kChunk);
   const Tin* target = static_cast<const Tin*>(a.target);
   const Tin* base = static_cast<const Tin*>(a.base);
   const Tin* W1 = static_cast<const Tin*>(a.W1);
   const Tin* W2 = static_cast<const Tin*>(a.W2);
+  float4* rowstat = ws_at<float4>(ws, L.rowstat);
+  int4* pend = ws_at<int4>(ws, L.pend);
+  float2* rpart = ws_at<float2>(ws, L.rpart);
+  resid_partials_kernel<Tin><<<dim3(nc, ceil_div(a.R, kRRows)), 256, 0, s>>>(
+      a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats, rowstat, pend, kT, rpart);
+  resid_locate_kernel<Tin><<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats,
+                                               rowstat, pend, kT, a.seed, rpart, a.out_tokens);
+  launches += 2;
+  return cudaGetLastError();
+}
+
+template <class Tin>
+static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s, int& launches) {
+  const WsLayout L = ws_layout(a.R, a.gamma, a.V);
+  void* ws = a.ws;
+  const int greedy = a.temperature == 0.f;
+  const float kT = greedy ? 0.f : (float)(1.4426950408889634 / (double)a.temperature);
   // the chain stages W1[prev] for the Markov head; the gated head's rows come next
   const int stage_rank = (sizeof(Tin) == 2 && !a.gate && a.rank % 64 == 0 && a.rank <= 256 &&
                           (reinterpret_cast<uintptr_t>(a.W1) & 15) == 0) ? a.rank : 0;
-  verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma + 1), kVsThreads, 0, s>>>(
-      a.R, a.gamma, a.V, target, a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy, a.seed,
-      ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount), ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
-      rowstat, a.p_tok, a.out_tokens, a.accepted_len, pend, status, W1, stage_rank,
-      ws_at<__nv_bfloat16>(ws, L.astage), 0);
-  launches += 1;
-  if (!greedy) {
-    if (a.gate) {
-      gated_stage_kernel<<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, a.anchor, a.tokens,
-                                             static_cast<const __nv_bfloat16*>(a.W1),
-                                             static_cast<const __nv_bfloat16*>(a.gate), pend,
-                                             ws_at<__nv_bfloat16>(ws, L.astage));
-      launches += 1;
-    }
-    bool taken = false;
-    cudaError_t e = launch_resid_persistent(a, s, launches, taken);
-    if (taken || e != cudaSuccess) return e == cudaSuccess ? cudaGetLastError() : e;
-    // the fallback kernels below recompute the Markov bias; the gated head
-    // was admitted only where the tensor-core pass runs
-    if (a.gate) return cudaErrorNotSupported;
-    const int nc = ceil_div(a.V, kChunk);
-    resid_partials_kernel<Tin><<<dim3(nc, ceil_div(a.R, kRRows)), 256, 0, s>>>(
-        a.R, a.gamma, a.V, a.rank, target, base, W1, W2, a.q_stats, rowstat, pend, kT, rpart);
-    resid_locate_kernel<Tin><<<a.R, 256, 0, s>>>(a.R, a.gamma, a.V, a.rank, target, base, W1, W2,
-                                                 a.q_stats, rowstat, pend, kT, a.seed, rpart,
-                                                 a.out_tokens);
-    launches += 2;
+  if (sizeof(Tin) == 2 && (a.V & 7) == 0 && (reinterpret_cast<uintptr_t>(a.target) & 15) == 0) {
+    verify_rows_warp_kernel<<<dim3(a.R, a.gamma + 1), 32 * kVwSplit, 0, s>>>(
+        a.R, a.gamma, a.V, static_cast<const __nv_bfloat16*>(a.target), a.tokens, a.anchor, a.q_tok, a.sched_len,
+        kT, greedy, a.seed, ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1),
+        ws_at<float4>(ws, L.rowstat), a.p_tok, a.out_tokens, a.accepted_len, ws_at<int4>(ws, L.pend),
+        ws_at<uint32_t>(ws, L.status), static_cast<const __nv_bfloat16*>(a.W1), stage_rank,
+        ws_at<__nv_bfloat16>(ws, L.astage));
+    launches += 1;
+    return launch_verify_tail_t<Tin>(a, s, launches);
   }
-  return cudaGetLastError();
+  verify_rows_kernel<Tin><<<dim3(kVsSplit, a.R, a.gamma + 1), kVsThreads, 0, s>>>(
+      a.R, a.gamma, a.V, static_cast<const Tin*>(a.target), a.tokens, a.anchor, a.q_tok, a.sched_len, kT, greedy,
+      a.seed, ws_at<float4>(ws, L.vsplit), ws_at<unsigned int>(ws, L.vcount),
+      ws_at<unsigned int>(ws, L.vcount) + (size_t)a.R * (a.gamma + 1), ws_at<float4>(ws, L.rowstat), a.p_tok,
+      a.out_tokens, a.accepted_len, ws_at<int4>(ws, L.pend), ws_at<uint32_t>(ws, L.status),
+      static_cast<const Tin*>(a.W1), stage_rank, ws_at<__nv_bfloat16>(ws, L.astage), 0);
+  launches += 1;
+  return launch_verify_tail_t<Tin>(a, s, launches);
 }
 
 // ---------------------------------------------------------------------------
@@ -705,6 +704,11 @@ cudaError_t launch_labels(const LabelArgs& a, cudaStream_t s, int& launches, boo
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int& launches) {
   if (a.dtype == DSPARK_BF16) return launch_verify_t<__nv_bfloat16>(a, s, launches);
   return launch_verify_t<float>(a, s, launches);
+}
+
+cudaError_t launch_verify_tail(const VerifyArgs& a, cudaStream_t s, int& launches) {
+  if (a.dtype == DSPARK_BF16) return launch_verify_tail_t<__nv_bfloat16>(a, s, launches);
+  return launch_verify_tail_t<float>(a, s, launches);
 }
 
 }  // namespace dspark

@@ -44,9 +44,9 @@ def test_gated_round_parity(R, gamma, V, rank, T):
     o = oracle_round(cfg, list(range(R)))
     rep = compare(cfg, g, o, list(range(R)))
     assert rep["positions"] > 0
-    # draft sweep with the round's schedule, row stats, and (sampled) the state staging and the residual
-    # sweep
-    assert g["launches"] == (4 if T > 0 else 2), g["launches"]
+    # the drafting launch (with the round's schedule, the row statistics and the chains) and, sampled, the
+    # state staging and the residual sweep
+    assert g["launches"] == (3 if T > 0 else 1), g["launches"]
 
 
 def test_gated_uses_the_prefix():
