@@ -367,6 +367,61 @@ __device__ bool row_stats_cta(const PersistParams& p, int ew, int lane, unsigned
   return ok;
 }
 
+// The CTAs past the sweep's, concurrently with it (they take part in none of its barriers). CTA n_cta is
+// the scheduler ("Verificação com agendamento por confiança"): the whole prefix schedule with every thread
+// of the block, then the list of the target rows verification reads. With verification in the launch, it
+// and the CTAs after it then stream those rows' statistics, one piece per warp. Out of line, like
+// after_sweep_work: the sweep's own code stays compact in the instruction caches.
+__device__ __noinline__ void side_cta_work(const PersistParams& pg, unsigned char* smem) {
+  // a local copy: the fields used stay in registers (through the parameter's address they would be read
+  // again after every memory-clobbering barrier and wait)
+  const PersistParams p = pg;
+  if (blockIdx.x == (unsigned)p.n_cta) {
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSchedCntBytes);
+    unsigned long long* shu = reinterpret_cast<unsigned long long*>(smem + kSchedCntBytes + kSchedKeysBytes);
+    double* shd = reinterpret_cast<double*>(shu + 32);
+    int* shi = reinterpret_cast<int*>(shd + 32);
+    const BlockSchedScratch sc{cnt, p.R * p.gamma <= kSmemKeys ? keys : nullptr, shu, shi, shd, shi + 32};
+    schedule_block(p.R, p.gamma, p.conf, p.conf_lag, p.sps, p.n_table, p.sched_mode, p.sched_len, p.sched_K,
+                   p.tau_theta, p.skey0, p.skey1, p.sidx0, p.sidx1, p.sched_fx, p.status, sc);
+    if (p.vfuse) list_scheduled_rows(p, shu);
+  }
+  if (p.vfuse) {  // every warp streams pieces through its own ring; the mbarriers follow the rings
+    const int w = (int)(threadIdx.x >> 5);
+    row_stats_warp(p, (int)(threadIdx.x & 31), smem + (size_t)w * kVwRingBytes,
+                   reinterpret_cast<uint64_t*>(smem + (size_t)kPWarps * kVwRingBytes) + w * kVwSlots);
+  }
+}
+
+// A sweep CTA's epilogue warps after the last draw (every CTA has drawn its tokens: the step loop ended at a
+// grid barrier whose verdict, the same for every warp, the caller tested). The rows still queued: warp ew's
+// ring is the ew-th 16 KB of the W2 and base rings (their copies have all landed: every stage was
+// consumed), its mbarriers in the uniforms table (read by the draws only), the claim words at the
+// dependency scratch. Then each warp runs the verification chain of requests blockIdx.x + ew n_cta,
+// blockIdx.x + (ew + 8) n_cta, ... once their rows are combined. `bars` is the 1 KB block after the rings.
+__device__ __noinline__ void after_sweep_work(const PersistParams& pg, int ew, int lane, unsigned char* sB,
+                                              unsigned char* bars) {
+  const PersistParams p = pg;  // a local copy, as in side_cta_work
+  if (!row_stats_cta(p, ew, lane, sB + (size_t)ew * kVwRingBytes,
+                     reinterpret_cast<uint64_t*>(bars + kOddOffset) + ew * kVwSlots,
+                     reinterpret_cast<volatile unsigned int*>(bars + kDepOffset)))
+    return;
+  for (int r = (int)blockIdx.x + ew * p.n_cta; r < p.R; r += kPEpiWarps * p.n_cta) {
+    const int L = min(max(__ldcg(p.sched_len + r), 0), p.gamma);
+    int ok = 1;
+    if (lane == 0) {
+      ok = wait_count(p.req_cnt + r, (unsigned int)(L + 1), p.status) ? 1 : 0;
+      if (ok) p.req_cnt[r] = 0u;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    if (!ok) break;
+    request_chain(r, p.gamma, p.V, p.target, p.tokens, p.anchor, p.q_tok, p.kT, p.greedy, p.seed, p.rowstat, p.p_tok,
+                  p.out_tokens, p.accepted_len, p.pend, p.status, p.W1, p.stage_rank, p.astage, L, lane);
+  }
+}
+
 }  // namespace dspark
 
 namespace dspark {
@@ -1102,7 +1157,7 @@ template <bool kResid, bool kLabel = false, bool kGated = false>
 __global__ void __launch_bounds__(kPThreads, 1)
     persistent_sweep_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                             const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapT,
-                            PersistParams p) {
+                            const __grid_constant__ PersistParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // drafting: A | 3 W2 stages | base ring; residual pass: A | 2 W2 stages |
@@ -1126,26 +1181,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   volatile int* sDecide = reinterpret_cast<volatile int*>(sTmem + 2);  // epilogue-group verdict
 
   if (!kResid && p.sched_on && blockIdx.x >= (unsigned)p.n_cta) {
-    // The CTAs past the sweep's, concurrently with it (they take part in none of its barriers). CTA n_cta
-    // is the scheduler ("Verificação com agendamento por confiança"): the whole prefix schedule with every
-    // thread of the block, then the list of the target rows verification reads. With verification in the
-    // launch, it and the CTAs after it then stream those rows' statistics, one piece per warp.
-    if (blockIdx.x == (unsigned)p.n_cta) {
-      uint32_t* cnt = reinterpret_cast<uint32_t*>(smem);
-      uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSchedCntBytes);
-      unsigned long long* shu = reinterpret_cast<unsigned long long*>(smem + kSchedCntBytes + kSchedKeysBytes);
-      double* shd = reinterpret_cast<double*>(shu + 32);
-      int* shi = reinterpret_cast<int*>(shd + 32);
-      const BlockSchedScratch sc{cnt, p.R * p.gamma <= kSmemKeys ? keys : nullptr, shu, shi, shd, shi + 32};
-      schedule_block(p.R, p.gamma, p.conf, p.conf_lag, p.sps, p.n_table, p.sched_mode, p.sched_len, p.sched_K,
-                     p.tau_theta, p.skey0, p.skey1, p.sidx0, p.sidx1, p.sched_fx, p.status, sc);
-      if (p.vfuse) list_scheduled_rows(p, shu);
-    }
-    if (p.vfuse) {  // every warp streams pieces through its own ring; the mbarriers follow the rings
-      const int w = (int)(threadIdx.x >> 5);
-      row_stats_warp(p, (int)(threadIdx.x & 31), smem + (size_t)w * kVwRingBytes,
-                     reinterpret_cast<uint64_t*>(smem + (size_t)kPWarps * kVwRingBytes) + w * kVwSlots);
-    }
+    side_cta_work(p, smem);
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1574,33 +1610,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (*sDecide) break;
       }
     }
-    // the rows still queued: epilogue warp ew's ring is the ew-th 16 KB of the W2 and base rings (their copies
-    // have all landed: every stage was consumed), its mbarriers in the uniforms table (read by the draws only).
-    // The test is the group's verdict of the last barrier, the same for every warp (a warp's own `stop` is
-    // not: the work below has named barriers).
-    if (!kResid && p.vfuse && !*sDecide &&
-        row_stats_cta(p, ew, lane, sB + (size_t)ew * kVwRingBytes,
-                      reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(bars) + kOddOffset) +
-                          ew * kVwSlots,
-                      reinterpret_cast<volatile unsigned int*>(reinterpret_cast<unsigned char*>(bars) + kDepOffset))) {
-      // every CTA has drawn its last tokens (the step loop ended at a grid barrier): each warp runs the
-      // verification chain of requests blockIdx.x + ew n_cta, blockIdx.x + (ew + 8) n_cta, ... once
-      // their rows are combined
-      for (int r = (int)blockIdx.x + ew * p.n_cta; r < p.R; r += kPEpiWarps * p.n_cta) {
-        const int L = min(max(__ldcg(p.sched_len + r), 0), p.gamma);
-        int ok = 1;
-        if (lane == 0) {
-          ok = wait_count(p.req_cnt + r, (unsigned int)(L + 1), p.status) ? 1 : 0;
-          if (ok) p.req_cnt[r] = 0u;
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        __syncwarp();
-        if (!ok) break;
-        request_chain(r, p.gamma, p.V, p.target, p.tokens, p.anchor, p.q_tok, p.kT, p.greedy, p.seed, p.rowstat,
-                      p.p_tok, p.out_tokens, p.accepted_len, p.pend, p.status, p.W1, p.stage_rank, p.astage, L,
-                      lane);
-      }
-    }
+    // the rows still queued and the chains; the test is the group's verdict of the last barrier, the same
+    // for every warp (a warp's own `stop` is not: the work has named barriers)
+    if (!kResid && p.vfuse && !*sDecide) after_sweep_work(p, ew, lane, sB, reinterpret_cast<unsigned char*>(bars));
     if (kResid) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
     if (et == 0 && a_phases > 0)  // nor an A box the MMA issuer stopped waiting for
       for (int ka = 0; ka < 4; ++ka) mbar_wait_drain(&aFull[ka], (a_phases - 1) & 1, p.status);
