@@ -333,13 +333,21 @@ __device__ __forceinline__ void request_chain(int r, int gamma, int V, const __n
                                               int32_t* __restrict__ acc_len, int4* __restrict__ pend,
                                               uint32_t* status, const __nv_bfloat16* __restrict__ W1, int stage_rank,
                                               __nv_bfloat16* astage, int L, int lane) {
-  const size_t rb = (size_t)r * (gamma + 1);
-  for (int k = lane; k < gamma; k += 32) {
-    float pv = 0.f;
+  // lane k of each block of 32 positions: the token, p and q of position k together, then the ratio test
+  // of position k + 1 on the values in registers (no round trip through p_tok)
+  const size_t rb = (size_t)r * (gamma + 1), tb = (size_t)r * gamma;
+  int A = L, x0 = 0;  // x0: this lane's drafted token of block 0 (positions 0..31), as stored
+  bool found = false;
+  for (int k0 = 0; k0 < gamma; k0 += 32) {
+    const int k = k0 + lane;
+    float pv = 0.f, qv = 1.f;
+    int xr = 0;
     if (k < L) {
-      int x = __ldcg(tokens + (size_t)r * gamma + k);
+      xr = __ldcg(tokens + tb + k);
+      int x = xr;
       if (x < 0 || x >= V) { set_status(status, DSPARK_ERR_RANGE); x = min(max(x, 0), V - 1); }
       const float4 rs = __ldcg(rowstat + rb + k);
+      qv = __ldcg(q_tok + tb + k);
       if (greedy) {
         pv = x == __float_as_int(rs.z) ? 1.f : 0.f;
       } else {
@@ -347,30 +355,27 @@ __device__ __forceinline__ void request_chain(int r, int gamma, int V, const __n
         pv = __fdiv_rn(ex2_approx(__fmaf_rn(t, kT, -__fmul_rn(rs.x, kT))), rs.y);
       }
     }
-    __stcg(p_tok + (size_t)r * gamma + k, pv);
-  }
-  __syncwarp();
-  int A = L;
-  for (int k0 = 1; k0 <= L; k0 += 32) {
-    const int kk = k0 + lane;
+    if (k < gamma) __stcg(p_tok + tb + k, pv);
+    if (k0 == 0) x0 = xr;
     bool fail = false;
-    if (kk <= L) {
-      const float pv = __ldcg(p_tok + (size_t)r * gamma + kk - 1);
-      const float qv = q_tok[(size_t)r * gamma + kk - 1];
-      const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)kk, kAccept);
+    if (k < L) {
+      const double u = philox_uniform(seed, (uint64_t)r, (uint64_t)(k + 1), kAccept);
       fail = !((qv <= 0.f) || (u < (double)pv / (double)qv));
     }
     const unsigned m = __ballot_sync(0xffffffffu, fail);
-    if (m) {  // the first rejected position k0 + ffs - 1 keeps A = k - 1 tokens
-      A = k0 + __ffs(m) - 2;
-      break;
+    if (!found && m) {  // the first rejected position k + 1 keeps A = k tokens
+      A = k0 + __ffs(m) - 1;
+      found = true;
     }
   }
   for (int kk = lane; kk <= gamma; kk += 32) {
-    if (kk < A) out[rb + kk] = __ldcg(tokens + (size_t)r * gamma + kk);
+    if (kk < A) out[rb + kk] = kk < 32 ? x0 : __ldcg(tokens + tb + kk);
     else if (kk > A) out[rb + kk] = -1;
   }
-  const int prev_raw = A ? __ldcg(tokens + (size_t)r * gamma + A - 1) : anchor[r];
+  int prev_raw;
+  if (A == 0) prev_raw = anchor[r];
+  else if (A <= 32) prev_raw = __shfl_sync(0xffffffffu, x0, A - 1);
+  else prev_raw = __ldcg(tokens + tb + A - 1);
   if (lane == 0) {
     acc_len[r] = A;
     if (greedy) {
