@@ -256,7 +256,8 @@ def label_bytes(cfg):
 # The sources the kernels with recorded DRAM traffic (the drafting sweep and its residual mode) are
 # compiled from: a change to any of them voids the record; host-only files (api.cu, the header's
 # declarations) do not.
-TRAFFIC_SOURCES = ("common.cuh", "draft_persistent.cu", "internal.h", "sched_common.cuh", "tc_ptx.cuh")
+TRAFFIC_SOURCES = ("common.cuh", "draft_persistent.cu", "internal.h", "sched_common.cuh", "tc_ptx.cuh",
+                   "verify_common.cuh")
 
 
 def csrc_digest():
