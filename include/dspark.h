@@ -370,7 +370,9 @@ dspark_status dspark_copy_scheduled_rows(int32_t R, int32_t gamma, int32_t V, in
 /*
  * Self-test of the bounded device waits: runs one wait of the kinds the
  * kernels use on a condition nothing meets -- `which` 0 = the grid barrier,
- * 1 = an mbarrier wait -- so that it gives up after its iteration limit
+ * 1 = an mbarrier wait, 2 = the poll on a counter another CTA of the launch
+ * advances (the drafting launch's row list and per-request completion) -- so
+ * that it gives up after its iteration limit
  * (about a second), records DSPARK_ERR_TIMEOUT in the workspace's status word
  * (read with dspark_device_status) and returns. Nothing traps; later calls on
  * the same context work. Uses word 16 of the workspace's status block.

@@ -1770,7 +1770,8 @@ namespace dspark {
 
 // Runs one of the kernels' bounded waits on a condition that nothing ever
 // meets, so that it gives up: `which` 0 = the grid barrier (a counter target
-// no launch reaches), 1 = an mbarrier phase that no arrival completes. The
+// no launch reaches), 1 = an mbarrier phase that no arrival completes, 2 = the
+// acquire poll on a counter another CTA advances (a target no one reaches). The
 // wait records DSPARK_ERR_TIMEOUT in the status word and the kernel returns;
 // nothing traps and the context stays usable.
 __global__ void wait_selftest_kernel(int which, uint32_t* status, unsigned int* counter) {
@@ -1780,6 +1781,8 @@ __global__ void wait_selftest_kernel(int which, uint32_t* status, unsigned int* 
   abort_flag = 0;
   if (which == 0) {
     grid_barrier(counter, 0xFFFFFFFFu, status, &abort_flag);
+  } else if (which == 2) {
+    wait_count(counter, 0xFFFFFFFFu, status);  // the poll on another CTA's counter (row list, rows done)
   } else {
     mbar_init(&bar, 1);
     mbar_fence_init();
@@ -1957,7 +1960,7 @@ cudaError_t launch_label_persistent(const LabelArgs& a, cudaStream_t s, int& lau
 
 extern "C" dspark_status dspark_wait_selftest(int32_t which, void* workspace, size_t workspace_bytes,
                                               dspark_stream_t stream) {
-  if (which != 0 && which != 1) return DSPARK_ERR_INVALID_ARG;
+  if (which < 0 || which > 2) return DSPARK_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 || workspace_bytes < 256)
     return DSPARK_ERR_WORKSPACE;
   uint32_t* status = static_cast<uint32_t*>(workspace);

@@ -280,7 +280,7 @@ def copy_scheduled_rows(host_target, device_target, host_sched_len, stream=None)
 
 
 def wait_selftest(which, ws, stream=None):
-    """A bounded device wait (0: grid barrier, 1: mbarrier) on a condition nothing meets; it
+    """A bounded device wait (0: grid barrier, 1: mbarrier, 2: counter poll) on a condition nothing meets; it
     gives up and records ERR_TIMEOUT in the workspace's status word."""
     _check(lib.dspark_wait_selftest(int(which), _ptr(ws, _U8), ws.numel(), _stream(stream)), "dspark_wait_selftest")
 

@@ -356,3 +356,23 @@ def test_copy_scheduled_rows_copies_exactly_the_verified_rows():
     g_part = gpu_round(cfg, dict(inp, target=part))
     for key in ("out_tokens", "accepted_len", "p_tok", "sched_len"):
         assert np.array_equal(g_full[key], g_part[key]), key
+
+
+def test_unaligned_target_takes_the_separate_verification():
+    """A target tensor that is not 16-byte aligned (a view one element into a
+    larger buffer): the drafting launch leaves the row statistics to their own
+    launch (the quarter-row kernel, plain loads) and the residual draw to the
+    CUDA-core kernels, and the round still equals the oracle's."""
+    cfg = TC_SHAPE
+    inp = device_inputs(cfg)
+    t = inp["target"]
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    view = buf[1:1 + t.numel()].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 16 != 0
+    inp["target"] = view
+    g = gpu_round(cfg, inp)
+    rep = compare(cfg, g, oracle_round(cfg, list(range(cfg.R))), list(range(cfg.R)))
+    assert rep["positions"] > 0
+    # draft (with the schedule), row statistics with the chains, residual partials, residual draw
+    assert g["launches"] == 4, g["launches"]

@@ -1,5 +1,6 @@
 """Failure detection on the device without a fault: a bounded wait of each
-kind the kernels use (the grid barrier, an mbarrier wait) is made to run out
+kind the kernels use (the grid barrier, an mbarrier wait, the poll on a
+counter another CTA advances) is made to run out
 on a condition nothing meets; it records DSPARK_ERR_TIMEOUT in the status
 word, the kernel returns, and the context keeps working (a round afterwards
 is correct)."""
@@ -18,7 +19,7 @@ if torch.cuda.is_available():
     from speculative_decoding_draft_seq_gb300 import dspark
 
 
-@pytest.mark.parametrize("which", [0, 1], ids=["grid_barrier", "mbarrier"])
+@pytest.mark.parametrize("which", [0, 1, 2], ids=["grid_barrier", "mbarrier", "counter_poll"])
 def test_bounded_wait_times_out_and_the_context_stays_usable(which):
     ws = dspark.new_workspace(4, 4, 64, 8, dspark.FP32, 16, "cuda")
     t0 = time.time()
