@@ -109,7 +109,9 @@ __device__ __forceinline__ void verify_row_item(
   const size_t row = rowi * V;
   float am, Ms = 0.f, Zs = 0.f;
   int ai;
-  if (sizeof(Tin) == 2 && (V & 7) == 0) {  // 8-element groups, eight 16-byte loads in flight per thread
+  // 8-element groups by 16-byte loads: bf16 rows of a multiple of 8 elements in a 16-byte aligned tensor
+  const bool fast = sizeof(Tin) == 2 && (V & 7) == 0 && (reinterpret_cast<uintptr_t>(target) & 15) == 0;
+  if (fast) {  // eight 16-byte loads in flight per thread
     RowStat st;
     const uint4* p = reinterpret_cast<const uint4*>(target + row);
     const int ng = V >> 3, T = blockDim.x;
@@ -187,8 +189,7 @@ __device__ __forceinline__ void verify_row_item(
       if (q[i].z > bv || (q[i].z == bv && ii < bi)) { bv = q[i].z; bi = ii; }
       M = fmaxf(M, q[i].x);
     }
-    // the weight formula of the streaming pass that produced the quarters
-    const bool fast = sizeof(Tin) == 2 && (V & 7) == 0;
+    // the weight formula of the streaming pass that produced the quarters (`fast` above)
     auto wgt = [&](float t, float m) {
       return fast ? ex2_approx(__fmaf_rn(t, kT, -__fmul_rn(m, kT))) : target_weight(t, m, kT);
     };
