@@ -26,6 +26,30 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Packed helpers: the larger of each bf16 half; two float32 in one 64-bit
+// register and an fma on both halves (sm_100 and later).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f32x2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f32x2_fma(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// A group of eight bf16 -inf: the filler of a chunk's missing groups.
+__device__ __forceinline__ uint4 neg_inf_group() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+
 // Streaming row statistics of 8 consecutive bf16 values (one 16-byte load):
 // sampled mode keeps (max m, sum of 2^(t kT - m kT)) with a running rescale,
 // greedy mode keeps (max, lowest index of the max).
@@ -71,44 +95,43 @@ struct RowStat {
       ai = v0 + i;
     }
   }
-  // A lane's share of one chunk at once: groups u = 0..nv-1 of q (the rest
-  // ignored). Sampled mode takes the chunk's maximum first and rescales the
-  // running sum at most once, then adds the 64 terms as eight independent
-  // group sums combined in a fixed tree (no branch or long dependency chain
-  // between groups); greedy mode keeps the lowest index of the maximum, the
-  // groups being g0, g0 + 32, ... in order.
-  __device__ __forceinline__ void add_chunk_sampled(const uint4 (&q)[8], int nv, float kT) {
-    float gm[8];
+  // A lane's share of one chunk at once. Sampled mode: the groups past the
+  // chunk's end must hold bf16 -inf (neg_inf_group()), so that they add nothing.
+  // The chunk's maximum comes first, on the packed bf16 pairs (exact: bf16 to
+  // float32 is exact and keeps the order); the running sum is rescaled at most
+  // once; then the 64 terms 2^(t kT - m kT) are formed and added in float32
+  // pairs (fma.rn.f32x2: each half rounds as the scalar instruction would; the
+  // sum as an fma by 1.0), in four independent accumulators combined in a
+  // fixed tree. Greedy mode keeps the lowest index of the maximum, the groups
+  // being g0, g0 + 32, ... in order (only the first nv).
+  __device__ __forceinline__ void add_chunk_sampled(const uint4 (&q)[8], float kT) {
+    uint32_t mx = 0xFF80FF80u;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-      float t[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        t[2 * e] = __uint_as_float(w[e] << 16);
-        t[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-      }
-      gm[u] = u < nv ? fmaxf(max3(t[0], t[1], t[2]), max3(t[3], t[4], max3(t[5], t[6], t[7]))) : -INFINITY;
-    }
-    const float cm = fmaxf(fmaxf(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5])), fmaxf(gm[6], gm[7]));
+    for (int u = 0; u < 8; ++u) mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(q[u].x, q[u].y), bf16x2_max(q[u].z, q[u].w)));
+    const float cm = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+    if (cm == -INFINITY) return;  // nothing in this chunk (and m may still be -inf)
     if (cm > m) {
       s = m == -INFINITY ? 0.f : __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, cm), kT)));
       m = cm;
     }
     const float mk = __fmul_rn(m, kT);
-    float a[8];
+    const unsigned long long k2 = f32x2_pack(kT, kT), nmk2 = f32x2_pack(-mk, -mk), one2 = f32x2_pack(1.f, 1.f);
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-      float x0 = 0.f, x1 = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        x0 += ex2_approx(__fmaf_rn(__uint_as_float(w[e] << 16), kT, -mk));
-        x1 += ex2_approx(__fmaf_rn(__uint_as_float(w[e] & 0xffff0000u), kT, -mk));
+        float a0, a1;
+        f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u)), k2, nmk2),
+                     a0, a1);
+        acc[u & 3] = f32x2_fma(f32x2_pack(ex2_approx(a0), ex2_approx(a1)), one2, acc[u & 3]);
       }
-      a[u] = u < nv ? x0 + x1 : 0.f;
     }
-    s += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    float r[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f32x2_unpack(acc[i], r[2 * i], r[2 * i + 1]);
+    s += ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
   }
   __device__ __forceinline__ void add_chunk_greedy(const uint4 (&q)[8], int nv, int g0) {
 #pragma unroll
@@ -142,7 +165,7 @@ __device__ __forceinline__ float4 warp_row_piece(const __nv_bfloat16* __restrict
   auto load = [&](uint4 (&q)[8], int c0) {
     const int cnt = min(kVwChunk, len - c0);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) q[u] = lane + 32 * u < cnt ? __ldcs(src + c0 + lane + 32 * u) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < 8; ++u) q[u] = lane + 32 * u < cnt ? __ldcs(src + c0 + lane + 32 * u) : neg_inf_group();
   };
   if (len > 0) load(cur, 0);
   for (int c0 = 0; c0 < len; c0 += kVwChunk) {
@@ -150,7 +173,7 @@ __device__ __forceinline__ float4 warp_row_piece(const __nv_bfloat16* __restrict
     const int cnt = min(kVwChunk, len - c0);
     const int nv = cnt > lane ? (cnt - lane + 31) / 32 : 0;
     if (greedy) st.add_chunk_greedy(cur, nv, gb + c0 + lane);
-    else st.add_chunk_sampled(cur, nv, kT);
+    else st.add_chunk_sampled(cur, kT);
 #pragma unroll
     for (int u = 0; u < 8; ++u) cur[u] = nxt[u];
   }
@@ -216,9 +239,9 @@ __device__ __forceinline__ bool warp_row_piece_ring(const __nv_bfloat16* __restr
     const int nv = cnt > lane ? (cnt - lane + 31) / 32 : 0;
     uint4 q[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) q[u] = u < nv ? c4[lane + 32 * u] : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < 8; ++u) q[u] = u < nv ? c4[lane + 32 * u] : neg_inf_group();
     if (greedy) st.add_chunk_greedy(q, nv, gb + j * kVwChunk + lane);
-    else st.add_chunk_sampled(q, nv, kT);
+    else st.add_chunk_sampled(q, kT);
     ++n_done;
     __syncwarp();
     if (next < nch) issue();
