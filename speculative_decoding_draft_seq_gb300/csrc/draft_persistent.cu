@@ -1556,10 +1556,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
               for (int i = 8; i < 64; ++i) mq[i & 7] = fmaxf(mq[i & 7], l[i]);
               m = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
               const float mk = __fmul_rn(m, kT);
-              float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              // chain c = i & 7 adds the weights of i = c, c + 8, ... in order; the pairs (i, i + 1) of
+              // chains (c, c + 1) go through one f32x2 fma each (the argument; the sum as an fma by 1.0):
+              // the same operations, in the same order, as eight scalar chains
+              const unsigned long long k2 = f32x2_pack(kT, kT), nmk2 = f32x2_pack(-mk, -mk),
+                                       one2 = f32x2_pack(1.f, 1.f);
+              unsigned long long sq2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-              for (int i = 0; i < 64; ++i) sq[i & 7] += pweight(l[i], kT, mk);
-              ssum = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
+              for (int i = 0; i < 64; i += 2) {
+                float a0, a1;
+                f32x2_unpack(f32x2_fma(f32x2_pack(l[i], l[i + 1]), k2, nmk2), a0, a1);
+                sq2[(i & 7) >> 1] = f32x2_fma(f32x2_pack(px2(a0), px2(a1)), one2, sq2[(i & 7) >> 1]);
+              }
+              float s0, s1, s2, s3, s4, s5, s6, s7;
+              f32x2_unpack(sq2[0], s0, s1);
+              f32x2_unpack(sq2[1], s2, s3);
+              f32x2_unpack(sq2[2], s4, s5);
+              f32x2_unpack(sq2[3], s6, s7);
+              ssum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
             }
             const int r = mt * kPM + row;
             if (r < p.R)
