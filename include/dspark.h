@@ -235,7 +235,12 @@ dspark_status dspark_acceptance_labels(int32_t R, int32_t gamma, int32_t V, int3
  * One whole round: draft -> schedule -> verify on one stream, with no host
  * synchronisation in between (the scheduled lengths stay on the device).
  * Arguments are the union of the three calls above; the intermediate outputs
- * (draft_tokens, q_tok, q_stats, sched_len, K, tau_theta) are written too.
+ * (draft_tokens, q_tok, q_stats, sched_len, K, tau_theta) are written too,
+ * and every output equals, bit for bit, what the three calls give in turn.
+ * On the tensor-core path the drafting launch itself computes the schedule
+ * and, outside ALL mode, the target row statistics and acceptance chains
+ * (the target tensor 16-byte aligned), leaving one launch for the residual
+ * or bonus draw.
  */
 dspark_status dspark_round(int32_t R, int32_t gamma, int32_t V, int32_t rank, int32_t dtype,
                            const void* base_logits, const void* target_logits,
