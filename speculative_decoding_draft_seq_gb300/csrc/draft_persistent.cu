@@ -9,22 +9,29 @@
 //
 // One CTA per SM, each owning a contiguous range of 64-column chunks of the
 // vocabulary. Per step k:
-//   1. the epilogue warps gather A = W1[prev_r, :] (128 requests per M tile)
-//      into 128-byte-swizzled K-major shared memory;
+//   1. A = W1[prev_r, :] (128 requests per M tile) arrives in 128-byte-
+//      swizzled K-major shared memory by TMA from the rows the previous step's
+//      draws staged in the workspace (gathered by threads at k = 1);
 //   2. tcgen05 MMAs (one issuing thread) multiply A by TMA-loaded W2 tiles
 //      into TMEM; the epilogue warps add the TMA-loaded base logits and write
 //      per-(request, chunk) softmax partials (max, sum of 2^((l-max)log2e/T))
 //      or (max, argmax) for greedy decoding;
 //   3. grid barrier; the epilogue warps of CTA b draw the tokens of requests
-//      r = b, b + #CTAs, ...: float64 combination of the chunk partials,
-//      inverse CDF to a chunk, recompute of that chunk's 64 logits, float64
-//      prefix sum to the token;
+//      r = b, b + #CTAs, ...: an exact 2^-40 fixed-point scan of the chunk
+//      masses finds the crossing chunk, its 64 logits are recomputed and a
+//      fixed-point warp scan finds the token, whose W1 row is staged for
+//      step k + 1;
 //   4. grid barrier; the tokens are visible to every CTA for step k + 1.
 // The W2 and base-logit producers do not depend on the sampled tokens, so
 // they keep streaming across steps: the first tiles of step k + 1 load while
-// step k is being located. Every wait (mbarrier or grid barrier) is bounded:
-// when one runs out the kernel records DSPARK_ERR_TIMEOUT, winds down, lets
-// issued copies and MMAs land and frees its TMEM.
+// step k is being located. Inside a round the launch has CTAs past the sweep's:
+// one computes the round's prefix schedule and lists the target rows
+// verification reads, and the others stream those rows' statistics; after the
+// last draw the sweep CTAs take the rows left and run the acceptance chains
+// (side_cta_work, after_sweep_work). Every wait (mbarrier, grid barrier,
+// counter poll) is bounded: when one runs out the kernel records
+// DSPARK_ERR_TIMEOUT, winds down, lets issued copies and MMAs land and frees
+// its TMEM.
 #include "common.cuh"
 #include "internal.h"
 #include "sched_common.cuh"

@@ -7,12 +7,16 @@
 // K from the confidences of two steps earlier by an unconstrained search, then
 // the top K of the current ranking).
 //
-// One CTA of 1024 threads (the problem is at most 65536 keys and latency
-// bound): survival products per request in float32, a stable LSD radix sort of
-// 32-bit keys (4-bit digits, per-thread contiguous segments, counts scanned in
-// digit-major order) with the flat candidate index as payload, an exact
-// fixed-point (2^-40) inclusive scan of the sorted survivals, and the
-// Theta_i comparisons in float64 with the operation order fixed by the C ABI.
+// Two forms. Up to 4,096 candidates, schedule_small_kernel: up to one CTA per
+// SM, each building every survival key and ranking its own candidates by
+// counting (below). Larger problems, schedule_kernel: schedule_block
+// (sched_common.cuh) in one CTA of 1024 threads -- survival products per
+// request in float32, a stable LSD radix sort of 32-bit keys (4-bit digits,
+// per-thread contiguous segments, counts scanned in digit-major order) with
+// the flat candidate index as payload, an exact fixed-point (2^-40) inclusive
+// scan of the sorted survivals, and the Theta_i comparisons in float64 with the
+// operation order fixed by the C ABI. Inside dspark_round on the tensor-core
+// path, one extra CTA of the drafting launch runs schedule_block instead.
 #include "common.cuh"
 #include "internal.h"
 #include "sched_common.cuh"

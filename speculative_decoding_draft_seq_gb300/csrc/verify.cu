@@ -4,15 +4,21 @@
 // the longest prefix consistent with the target distribution; decoding-cycle
 // paragraph: E and F accepted, G rejected, corrected token G* emitted).
 //
-// Launches:
-//   verify_rows_kernel  one CTA per quarter of each scheduled target row
-//                  (r, k <= L_r): streams it once with 128-bit loads (online
-//                  max / sum of 2^((t - m) log2(e) / T)); the last quarter of a
-//                  row combines the four (M, Z, argmax) and writes
-//                  p_tok = P_k(x_{k+1}); the last row of a request runs its
-//                  chain of ratio tests u < p / q, records the pending
+// Launches (inside dspark_round on the tensor-core path, outside ALL mode, the
+// row statistics and chains run in the drafting launch instead, with the same
+// functions: verify_common.cuh):
+//   verify_rows_warp_kernel  bf16 rows of a multiple of 8 elements in a
+//                  16-byte aligned tensor: one CTA of eight warps per scheduled
+//                  target row (r, k <= L_r), warp w streaming the row's w-th
+//                  eighth (online max / sum of 2^((t - m) log2(e) / T)); the CTA
+//                  combines the eight into (M, Z, argmax), and the CTA that
+//                  combines a request's last row runs its chain of ratio tests
+//                  u < p / q (p_tok = P_k(x_{k+1})), records the pending
 //                  residual (first rejection j = A + 1) or bonus draw (row
 //                  L_r = A), and stages the A row of the residual's Q_j.
+//   verify_rows_kernel  any dtype or width (and the labels' statistics): one
+//                  CTA per quarter row, the last quarter combining the four,
+//                  the same chain.
 //   gated_stage_kernel  (recurrent head only) the A row bf16(s_j), the state
 //                  replayed over the anchor and the accepted tokens.
 //   the residual / bonus draw: the tensor-core sweep in residual mode
