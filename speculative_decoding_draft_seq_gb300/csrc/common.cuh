@@ -93,7 +93,6 @@ __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, size_t i) {
   const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p) + i);
   return __uint_as_float(((uint32_t)b) << 16);
 }
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
 // ---------------------------------------------------------------------------
 // Recurrent (gated) sequential head ("Head RNN" of the GeekNews page): state
@@ -186,11 +185,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     const int oi = __shfl_xor_sync(0xffffffffu, i, o);
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
-}
-__device__ __forceinline__ int warp_sum_i(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 __device__ __forceinline__ int warp_min_i(int v) {
 #pragma unroll

@@ -187,26 +187,6 @@ __device__ __forceinline__ float resid_w(int kind, float t, float l, const Resid
 // --- reductions over the 8 epilogue warps (named barrier 1) --------------
 __device__ __forceinline__ void eg_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__device__ __forceinline__ float eg_max(float v, float* sh, int ew, int lane) {
-  v = warp_max(v);
-  if (lane == 0) sh[ew] = v;
-  eg_sync();
-  float r = sh[0];
-#pragma unroll
-  for (int i = 1; i < kPEpiWarps; ++i) r = fmaxf(r, sh[i]);
-  eg_sync();
-  return r;
-}
-__device__ __forceinline__ int eg_min_i(int v, int* sh, int ew, int lane) {
-  v = warp_min_i(v);
-  if (lane == 0) sh[ew] = v;
-  eg_sync();
-  int r = sh[0];
-#pragma unroll
-  for (int i = 1; i < kPEpiWarps; ++i) r = min(r, sh[i]);
-  eg_sync();
-  return r;
-}
 __device__ __forceinline__ int eg_max_i(int v, int* sh, int ew, int lane) {
   v = warp_max_i(v);
   if (lane == 0) sh[ew] = v;

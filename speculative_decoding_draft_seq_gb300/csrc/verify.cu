@@ -57,23 +57,6 @@ __device__ __forceinline__ float target_weight(float t, float m, float kT) {
 struct OnlineStat {
   float m = -INFINITY, s = 0.f, am = -INFINITY;
   int ai = 0x7fffffff;
-  __device__ __forceinline__ void add8(const float (&t)[8], int v0, float kT, bool greedy) {
-    float gm = t[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) gm = fmaxf(gm, t[i]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (t[i] > am) { am = t[i]; ai = v0 + i; }  // strict: keeps the first index of a tie
-    if (greedy) return;
-    if (gm > m) {
-      s = __fmul_rn(s, target_weight(m, gm, kT));
-      m = gm;
-    }
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) part += target_weight(t[i], m, kT);
-    s += part;
-  }
   __device__ __forceinline__ void add1(float t, int v, float kT, bool greedy) {
     if (t > am) { am = t; ai = v; }
     if (greedy) return;

@@ -105,3 +105,54 @@ def test_gated_mixed_domain(T):
     requests = list(range(0, cfg.R, 4))
     g = gpu_round(cfg)
     compare(cfg, g, oracle_pool.oracle_round(cfg, requests), requests)
+
+
+def _separate_calls(cfg, inp):
+    """The round as three separate C-ABI calls: dspark_draft_sequential_gated,
+    dspark_schedule and dspark_verify_gated, on one workspace and stream."""
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dspark.BF16, inp["sps"].numel())
+    out = dspark.RoundOutputs(R, gamma)
+    dspark.draft_sequential_gated(inp["base"], inp["anchor"], inp["W1"], inp["gate"], inp["W2"], inp["T"],
+                                  inp["seed"], out.tokens, out.q_tok, out.q_stats, ws)
+    dspark.schedule(inp["conf"], inp["conf_lag"], inp["sps"], inp["mode"], out.sched_len, out.K, out.tau_theta, ws)
+    dspark.verify_gated(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["gate"], inp["W2"], out.tokens,
+                        out.q_tok, out.q_stats, out.sched_len, inp["T"], inp["seed"], out.out_tokens,
+                        out.accepted_len, out.p_tok, ws)
+    res = out.host()
+    res["status"] = dspark.device_status(ws)
+    return res
+
+
+# (R, gamma, V, rank, mode, T): two M tiles with a vocabulary tail, both admission modes, greedy, full rank
+SEPARATE = [(150, 4, 3000, 64, W.CAUSAL, 1.0), (150, 4, 3000, 64, W.LAGGED, 1.0), (150, 4, 3000, 64, W.CAUSAL, 0.0),
+            (64, 5, 4104, 256, W.CAUSAL, 1.0)]
+
+
+@pytest.mark.parametrize("R,gamma,V,rank,mode,T", SEPARATE)
+def test_gated_separate_calls_equal_the_round(R, gamma, V, rank, mode, T):
+    """The stages called one by one (the gated drafting, the scheduler, the
+    gated verification with its state replay for the residual draws) give
+    every output of dspark_round_gated bit for bit, and match the oracle."""
+    cfg = W.with_(_cfg(R, gamma, V, rank, T), mode=mode)
+    inp = device_inputs(cfg)
+    s = _separate_calls(cfg, inp)
+    assert s["status"] == dspark.OK, dspark.status_string(s["status"])
+    g = gpu_round(cfg, inp)
+    for k in ("tokens", "q_tok", "q_stats", "sched_len", "K", "tau_theta", "out_tokens", "accepted_len", "p_tok"):
+        assert np.array_equal(s[k], g[k]), k
+    requests = list(range(R))
+    rep = compare(cfg, s, oracle_pool.oracle_round(cfg, requests), requests)
+    assert rep["positions"] > 0
+
+
+def test_gated_separate_calls_full_size():
+    """The same equality at DeepSeek scale (R = 128, gamma = 16, V = 129,280,
+    rank 256), where the round verifies inside its drafting launch."""
+    cfg = W.with_(W.CONFIGS["ds"], gated=True)
+    inp = device_inputs(cfg)
+    s = _separate_calls(cfg, inp)
+    assert s["status"] == dspark.OK, dspark.status_string(s["status"])
+    g = gpu_round(cfg, inp)
+    for k in ("tokens", "q_tok", "q_stats", "sched_len", "K", "tau_theta", "out_tokens", "accepted_len", "p_tok"):
+        assert np.array_equal(s[k], g[k]), k

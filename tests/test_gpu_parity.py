@@ -376,3 +376,26 @@ def test_unaligned_target_takes_the_separate_verification():
     assert rep["positions"] > 0
     # draft (with the schedule), row statistics with the chains, residual partials, residual draw
     assert g["launches"] == 4, g["launches"]
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0], ids=["sampled", "greedy"])
+def test_full_size_separate_calls_equal_the_round(T):
+    """At DeepSeek scale dspark_round verifies inside its drafting launch (the
+    scheduler CTA, the row-statistics CTAs, the chains after the last draw);
+    dspark_draft_sequential, dspark_schedule and dspark_verify called one by
+    one must give every one of its outputs bit for bit."""
+    cfg = W.with_(W.CONFIGS["ds"], T=T)
+    inp = device_inputs(cfg)
+    R, gamma, V = inp["base"].shape
+    ws = dspark.new_workspace(R, gamma, V, cfg.rank, dspark.BF16, inp["sps"].numel())
+    out = dspark.RoundOutputs(R, gamma)
+    dspark.draft_sequential(inp["base"], inp["anchor"], inp["W1"], inp["W2"], inp["T"], inp["seed"], out.tokens,
+                            out.q_tok, out.q_stats, ws)
+    dspark.schedule(inp["conf"], inp["conf_lag"], inp["sps"], inp["mode"], out.sched_len, out.K, out.tau_theta, ws)
+    dspark.verify(inp["target"], inp["base"], inp["anchor"], inp["W1"], inp["W2"], out.tokens, out.q_tok,
+                  out.q_stats, out.sched_len, inp["T"], inp["seed"], out.out_tokens, out.accepted_len, out.p_tok, ws)
+    assert dspark.device_status(ws) == dspark.OK
+    s = out.host()
+    g = gpu_round(cfg, inp)
+    for k in ("tokens", "q_tok", "q_stats", "sched_len", "K", "tau_theta", "out_tokens", "accepted_len", "p_tok"):
+        assert np.array_equal(s[k], g[k]), k
