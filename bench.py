@@ -695,8 +695,11 @@ def main():
         "round_us_direct_call": None if direct_ms is None else direct_ms * 1e3,
         "round_us_p10_median_p90": [pct[10], pct[50], pct[90]],
         "stages_us": {"draft": t_draft * 1e3, "schedule": t_sched * 1e3, "verify": t_verify * 1e3},
-        "stages_note": ("each entry point timed alone; inside dspark_round one extra CTA of the drafting "
-                        "launch computes the schedule while the other CTAs sweep (no launch of its own)"),
+        "stages_note": ("each entry point timed alone (verify: its row-statistics launch and its residual "
+                        "launch; roofline.verify_frac is this standalone call); inside dspark_round one extra "
+                        "CTA of the drafting launch computes the schedule and a few more stream the scheduled "
+                        "target rows' statistics while the other CTAs sweep, its sweep CTAs run the acceptance "
+                        "chains after the last draw, and the residual draw is the round's second launch"),
         "sts": {"fit_us": t_sts_fit * 1e3, "fit_rows": n_sts, "grid": 64, "bins": 15,
                 "apply_us": t_sts_apply * 1e3},
         "gated_head": gated,
