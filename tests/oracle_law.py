@@ -9,8 +9,6 @@ outcome alone, without re-computing any probability the oracle computes. A
 depth-first walk over decisions then yields every possible emitted sequence
 with its exact probability (to the bisection width, 1e-14).
 """
-import numpy as np
-
 from oracle import draft as D, verify as Vf, gated as G, philox
 
 EPS = 1e-15

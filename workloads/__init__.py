@@ -25,7 +25,7 @@ full tensors directly in HBM. Small tensors (anchors, confidences, tables,
 rank permutations) come from numpy PCG64 streams and are copied to the device.
 """
 
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 import math
 import statistics
 
