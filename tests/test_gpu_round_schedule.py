@@ -167,13 +167,16 @@ def test_round_schedule_nonfinite_table(mode, where):
     assert gpu_round(cfg, inp)["status"] == dspark.ERR_NONFINITE
 
 
+@pytest.mark.parametrize("R,gamma,n_table,table", [(600, 14, 8800, "concave"), (4096, 16, 69632, "step")],
+                         ids=["8400", "65536"])
 @pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
-def test_round_schedule_sort_in_workspace(mode):
+def test_round_schedule_sort_in_workspace(mode, R, gamma, n_table, table):
     """8,400 candidates, more than the scheduler CTA's shared memory holds:
     its radix sort runs through the workspace's buffers, still inside the
-    drafting launch."""
-    cfg = _cfg(600, 14, 128, mode, 8800)
-    inp, conf, lag, sps = _tie_inputs(cfg, "concave")
+    drafting launch; and the largest round the scheduler takes (65,536
+    candidates, 4,096 requests in 32 M tiles)."""
+    cfg = _cfg(R, gamma, 128, mode, n_table)
+    inp, conf, lag, sps = _tie_inputs(cfg, table)
     g = gpu_round(cfg, inp)
     assert g["status"] == dspark.OK, dspark.status_string(g["status"])
     assert g["launches"] == (3 if mode == W.ALL else 2), g["launches"]

@@ -2,7 +2,8 @@
 exact ties in the prefix survivals (confidences drawn from a few values,
 including 0 and 1) -- the case where the order of equal keys decides which
 candidates are admitted. Covers both device forms: the rank-and-admit pair
-(R * gamma <= 4096) and the single-CTA radix sort (larger problems).
+(R * gamma <= 4096) and the single-CTA radix sort (larger problems, up to the
+entry point's maximum of 65,536 candidates).
 """
 import numpy as np
 import pytest
@@ -33,7 +34,9 @@ def _conf(R, gamma, rng):
 CASES = [(40, 5, 260, "concave"), (128, 16, 2200, "step"), (256, 16, 4400, "cliff"),
          (300, 20, 6400, "concave"), (1, 1, 4, "step"), (7, 3, 9, "cliff"),
          # more than 8192 keys: the radix sort runs through the workspace (scheduler-stress size)
-         (1024, 16, 17408, "step"), (1024, 16, 16384, "cliff")]
+         (1024, 16, 17408, "step"), (1024, 16, 16384, "cliff"),
+         # the largest problem the entry point takes, R * gamma = 65,536, in three shapes
+         (4096, 16, 69632, "step"), (2048, 32, 65536, "cliff"), (65536, 1, 98304, "cliff")]
 
 
 @pytest.mark.parametrize("R,gamma,n_table,table", CASES)
